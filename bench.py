@@ -1,0 +1,359 @@
+#!/usr/bin/env python
+"""Benchmark of causal context-parallel attention on one GB300.
+
+Workload (default): ring attention forward, MHA, S=8192, H=32, D=128, bf16,
+q/k/v ~ N(0,1) (seed 0), causal, P=8 virtual ranks, zigzag (dual-chunk-swap)
+layout, fused ring schedule.  One step is one pass of the hot path over that
+input: zigzag reorder of q, k, v into the ranks' layout, the ring attention
+(one tcgen05 kernel walking every rank's key/value blocks in ring order, with
+the log-sum-exp merge in its online softmax), and the restore of out and lse
+to sequence order.  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (256 MiB write) between timed steps.
+
+Prints ONE JSON line.  ``--impl reference`` times the CPU float64 oracle (the
+correctness reference) on a bounded sample of the same workload instead.
+Under torchrun with N>1 every rank runs the same workload on its own GPU
+(replicas: the method has no cross-GPU step here) and rank 0 reports
+N x work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal CP-attn TFLOP/s (fwd, fwd+bwd) & permute GB/s, % of roofline, 1 GB300"
+WORKLOAD = "ring_fwd_mha_s8192_h32_d128_bf16_p8_zigzag"
+S, H, D, P = 8192, 32, 128, 8
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def causal_flop(S: int, H: int, D: int) -> float:
+    """4*D FLOP per visible (query, key) pair per head (QK^T and PV)."""
+    return 4.0 * D * H * (S * (S + 1) // 2)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def _traffic_record(kernel_key: str):
+    """DRAM bytes per launch of a kernel from a committed ncu capture, or None
+    when the kernel's source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel_key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != rec.get("source_sha256_16"):
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_start - 1 <= r[0] <= self.t_end + 1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def cpu_oracle_sample(q, k, v, target_s: float = 12.0):
+    """Times the float64 oracle on sampled query rows (all heads) of the workload.
+    Returns (TFLOP/s, rows, seconds)."""
+    import oracle
+
+    rng = np.random.default_rng(123)
+    qs = q.float().numpy().astype(np.float64)
+    ks = k.float().numpy().astype(np.float64)
+    vs = v.float().numpy().astype(np.float64)
+
+    def run(n):
+        rows = np.sort(rng.integers(0, S, size=n))
+        t0 = time.perf_counter()
+        oracle.attention(qs[rows], ks, vs, True, pos_q=rows, pos_k=np.arange(S))
+        dt = time.perf_counter() - t0
+        flop = 4.0 * D * H * float(np.sum(rows + 1))
+        return flop, dt, n
+
+    flop, dt, n = run(8)
+    n2 = int(max(8, min(4096, 8 * target_s / max(dt, 1e-3))))
+    flop, dt, n = run(n2)
+    return flop / dt / 1e12, n, dt
+
+
+def bench_reference(args):
+    ws, rank = _dist()
+    if rank != 0:
+        return
+    from synth import make_inputs
+
+    q, k, v = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
+    per_step = []
+    rows_used = 0
+    for i in range(args.warmup + args.steps):
+        tf, n, dt = cpu_oracle_sample(q, k, v, target_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
+        if i >= args.warmup:
+            per_step.append((tf, dt))
+            rows_used = n
+    value = statistics.mean(t for t, _ in per_step)
+    ms = 1e3 * statistics.mean(d for _, d in per_step)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seed 0",
+        "config": {"workload": WORKLOAD, "S": S, "H": H, "D": D, "P": P, "reorder": "dual_chunk_swap"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_used} random query rows x {H} heads per step, full causal key range"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args):
+    import context_causal_attention_tcgen05_gb300 as cpa
+    from synth import make_inputs
+
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cpa.load_library()  # raises when the library is missing: there is no fallback
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    q_h, k_h, v_h = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    q_re, k_re, v_re = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    o_re, out = torch.empty_like(q), torch.empty_like(q)
+    lse_re = torch.empty(H, S, dtype=torch.float32, device=dev)
+    lse = torch.empty_like(lse_re)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    layout = "zigzag"
+
+    def step(ev):
+        ev[0].record(stream)
+        cpa.cp_zigzag_reorder(q, P, y=q_re)
+        cpa.cp_zigzag_reorder(k, P, y=k_re)
+        cpa.cp_zigzag_reorder(v, P, y=v_re)
+        ev[1].record(stream)
+        cpa.cp_ring_attention_reordered(q_re, k_re, v_re, P, layout, "fused", out=o_re, lse=lse_re)
+        ev[2].record(stream)
+        cpa.cp_zigzag_restore(o_re, P, x=out)
+        cpa.cp_lse_reorder(lse_re, P, layout, inverse=True, y=lse)
+        ev[3].record(stream)
+
+    launches_per_step = 6
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+    st = cpa.cp_check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {cpa.cp_last_error()}")
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.6)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    events = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)  # write > L2 between steps (outside the events)
+        ev = mk()
+        step(ev)
+        events.append(ev)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    sampler.mark_end()
+    clocks = sampler.finish()
+    st = cpa.cp_check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {cpa.cp_last_error()}")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in events]
+    perm_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in events]
+    mean_step = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([mean_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_step = float(t.item())
+    flop = causal_flop(S, H, D)
+    value = ws * flop / (mean_step * 1e-3) / 1e12
+    attn_mean = statistics.mean(attn_ms)
+    achieved = flop / (attn_mean * 1e-3) / 1e12
+    tensor_bytes = S * H * D * 2
+    perm_bytes = 3 * 2 * tensor_bytes + 2 * tensor_bytes + 2 * S * H * 4
+    perm_gbs = perm_bytes / (statistics.mean(perm_ms) * 1e-3) / 1e9
+
+    # end to end through the public one-call driver with host buffers
+    q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_p = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    wsz = cpa.cp_workspace_size("ring_fwd", S, H, H, D, torch.bfloat16, P, "fused")
+    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(q_p, non_blocking=True)
+        kd.copy_(k_p, non_blocking=True)
+        vd.copy_(v_p, non_blocking=True)
+        cpa.cp_ring_attention(qd, kd, vd, P, layout, "fused", out=out, lse=lse, workspace=work)
+        out_p.copy_(out, non_blocking=True)
+        lse_p.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        e2e_ms.append((a, b))
+    torch.cuda.synchronize()
+    e2e_mean = statistics.mean(a.elapsed_time(b) for a, b in e2e_ms)
+    if ws > 1:
+        t = torch.tensor([e2e_mean], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    e2e_value = ws * flop / (e2e_mean * 1e-3) / 1e12
+
+    if rank == 0:
+        peaks = _peaks()
+        peak = peaks["bf16_tflops"]
+        traffic = _traffic_record("attn_fwd_tc")
+        cpu_tf, cpu_rows, cpu_s = (None, 0, 0.0)
+        if not args.no_cpu_baseline:
+            cpu_tf, cpu_rows, cpu_s = cpu_oracle_sample(q_h, k_h, v_h)
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic N(0,1), seed 0",
+            "config": {"workload": WORKLOAD, "S": S, "H": H, "D": D, "P": P, "reorder": "dual_chunk_swap",
+                       "ring_mode": "fused", "l2": "flushed between timed steps (256 MiB write)"},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "attn_fwd_tc (ring, fused)", "peak_source": peaks["source"] + " burst bf16"},
+            "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,
+                      "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
+                      "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * tensor_bytes,
+                    "d2h_bytes_per_step": tensor_bytes + S * H * 4, "ms_per_step": e2e_mean},
+            "clocks": clocks,
+        }
+        if cpu_tf is not None:
+            line["cpu_baseline"] = {"value": cpu_tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                    "sample": f"{cpu_rows} random query rows x {H} heads, full causal key "
+                                              f"range ({cpu_s:.1f} s of float64 CPU work)"}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

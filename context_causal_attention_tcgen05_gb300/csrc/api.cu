@@ -1,0 +1,918 @@
+// C ABI (include/cp_attn.h): argument validation, workspace layout, and the
+// ring / Ulysses drivers over P virtual ranks held in one GPU's memory.
+//
+// Sources: handbook chapter "Context parallelism: Ring Attention and Ulysses"
+// (sections "Ulysses: transposing between the sequence and the heads", "Ring
+// Attention: passing the KV once around a ring", "The zigzag partition") and
+// the MaxText pull request "Add Packing Support for Context Parallelism (Ring
+// Attention) #2906" (reorder strategies; packing accepted only with a
+// load-balanced ring).
+//
+// On one GPU the ring's point-to-point KV pass is an index: at step s virtual
+// rank r reads the key/value rows of rank (r - s) mod P from the reordered
+// buffer.  The Ulysses all-to-all is the seq2head / head2seq permute kernel.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace cpa {
+
+static thread_local std::string g_last_error;
+
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+cp_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return CP_OK;
+  set_last_error(std::string(what) + ": " + cudaGetErrorString(e));
+  return CP_ERR_CUDA;
+}
+
+// The device error word: a kernel that gives up on a bounded wait records a
+// code here; cp_check_device_status reads and clears it.
+__device__ int32_t g_device_error = 0;
+
+static std::mutex g_err_mu;
+static int32_t* g_err_ptr[64] = {nullptr};
+
+int32_t* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int64_t schedule_units(Schedule& s, int tile_rows, int heads) {
+  int64_t tiles = 0;
+  for (int i = 0; i < s.n_groups; ++i) {
+    s.g[i].tile0 = (int32_t)tiles;
+    tiles += (s.g[i].nq + tile_rows - 1) / tile_rows;
+  }
+  return tiles * heads;
+}
+
+}  // namespace cpa
+
+using namespace cpa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+size_t dtype_size(int32_t dt) { return dt == CP_F32 ? 4 : 2; }
+
+#define CP_REQUIRE(cond, code, msg)   \
+  do {                                \
+    if (!(cond)) {                    \
+      set_last_error(msg);            \
+      return code;                    \
+    }                                 \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cp_status check_tensor(const void* p, const char* name, bool may_be_null_if_empty, bool empty) {
+  if (p == nullptr) {
+    if (may_be_null_if_empty && empty) return CP_OK;
+    set_last_error(std::string(name) + " is NULL");
+    return CP_ERR_INVALID_ARG;
+  }
+  if (!aligned16(p)) {
+    set_last_error(std::string(name) + " is not 16-byte aligned");
+    return CP_ERR_ALIGN;
+  }
+  return CP_OK;
+}
+
+#define CP_CHECK_T(p, name, empty)                                    \
+  do {                                                                \
+    cp_status _st = check_tensor((p), (name), true, (empty));         \
+    if (_st != CP_OK) return _st;                                     \
+  } while (0)
+
+#define CP_TRY(expr)               \
+  do {                             \
+    cp_status _st = (expr);        \
+    if (_st != CP_OK) return _st;  \
+  } while (0)
+
+cp_status check_common(int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype) {
+  CP_REQUIRE(dtype == CP_F32 || dtype == CP_BF16, CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  CP_REQUIRE(Hq >= 1 && Hkv >= 1, CP_ERR_INVALID_ARG, "head counts must be >= 1");
+  CP_REQUIRE(Hq % Hkv == 0, CP_ERR_SHAPE, "Hq must be a multiple of Hkv (grouped-query attention)");
+  if (dtype == CP_F32) {
+    CP_REQUIRE(D == 16 || D == 32 || D == 64 || D == 128, CP_ERR_SHAPE,
+               "D must be one of 16, 32, 64, 128");
+  } else {
+    CP_REQUIRE(D == 64 || D == 128, CP_ERR_DTYPE,
+               "bf16 attention (tcgen05 kernel) supports D = 64 or 128");
+  }
+  return CP_OK;
+}
+
+bool fits_i32(int64_t x) { return x >= -(int64_t)INT32_MAX && x <= (int64_t)INT32_MAX; }
+
+// One rank's run of rows in a reordered buffer with an affine position map.
+struct Piece {
+  int32_t row0, n, pos_off, pos_stride;
+};
+
+// Rank holdings for a ring layout, rows in the reordered buffer (rank-major).
+std::vector<std::vector<Piece>> rank_pieces(int64_t S, int32_t P, int32_t layout) {
+  std::vector<std::vector<Piece>> out(P);
+  if (layout == CP_REORDER_CONTIGUOUS) {
+    int32_t C = (int32_t)(S / P);
+    for (int r = 0; r < P; ++r) out[r].push_back({r * C, C, r * C, 1});
+  } else if (layout == CP_REORDER_DUAL_CHUNK_SWAP) {
+    int32_t C = (int32_t)(S / (2 * P));
+    for (int r = 0; r < P; ++r) {
+      out[r].push_back({2 * r * C, C, r * C, 1});
+      out[r].push_back({2 * r * C + C, C, (2 * P - 1 - r) * C, 1});
+    }
+  } else {  // striped
+    int32_t n = (int32_t)(S / P);
+    for (int r = 0; r < P; ++r) out[r].push_back({r * n, n, r, P});
+  }
+  return out;
+}
+
+int64_t piece_pos_max(const Piece& p) { return (int64_t)p.pos_off + (int64_t)p.pos_stride * (p.n - 1); }
+
+// Could any key of `k` be visible to any query of `q` under the causal rule?
+bool maybe_visible(const Piece& q, const Piece& k, int causal) {
+  if (q.n == 0 || k.n == 0) return false;
+  if (!causal) return true;
+  return k.pos_off <= piece_pos_max(q);
+}
+
+void add_group(Schedule& s, const Piece& q) {
+  QGroup& g = s.g[s.n_groups++];
+  memset(&g, 0, sizeof(g));
+  g.q_row0 = q.row0;
+  g.nq = q.n;
+  g.pos_off = q.pos_off;
+  g.pos_stride = q.pos_stride;
+  g.seg_begin = s.n_segs;
+  g.seg_count = 0;
+  g.lse_col0 = q.row0;
+  g.lse_head0 = 0;
+  g.o_row0 = q.row0;
+}
+
+void add_seg(Schedule& s, const Piece& k) {
+  KSeg& sg = s.s[s.n_segs++];
+  sg.k_row0 = k.row0;
+  sg.nk = k.n;
+  sg.pos_off = k.pos_off;
+  sg.pos_stride = k.pos_stride;
+  s.g[s.n_groups - 1].seg_count++;
+}
+
+// Heaviest group first (more key rows to visit), so long query tiles start early.
+void sort_groups_by_work(Schedule& s) {
+  std::vector<int> idx(s.n_groups);
+  std::vector<int64_t> w(s.n_groups, 0);
+  for (int i = 0; i < s.n_groups; ++i) {
+    idx[i] = i;
+    for (int k = 0; k < s.g[i].seg_count; ++k) w[i] += s.s[s.g[i].seg_begin + k].nk;
+    w[i] *= (int64_t)s.g[i].nq > 0 ? 1 : 0;
+  }
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return w[a] > w[b]; });
+  QGroup tmp[kMaxGroups];
+  for (int i = 0; i < s.n_groups; ++i) tmp[i] = s.g[idx[i]];
+  for (int i = 0; i < s.n_groups; ++i) s.g[i] = tmp[i];
+}
+
+// Ring schedule.  step < 0: every step (fused); else only that step.
+void build_ring_schedule(Schedule& s, int64_t S, int32_t P, int32_t layout, int step, int causal) {
+  auto pieces = rank_pieces(S, P, layout);
+  s.n_groups = 0;
+  s.n_segs = 0;
+  for (int r = 0; r < P; ++r) {
+    for (const Piece& q : pieces[r]) {
+      add_group(s, q);
+      for (int st = 0; st < P; ++st) {
+        if (step >= 0 && st != step) continue;
+        int src = ((r - st) % P + P) % P;
+        for (const Piece& k : pieces[src])
+          if (maybe_visible(q, k, causal)) add_seg(s, k);
+      }
+    }
+  }
+  sort_groups_by_work(s);
+}
+
+// Key-major schedule for the backward: one group per key piece, segments =
+// the query pieces that may see it.
+void build_ring_bwd_schedule(Schedule& s, int64_t S, int32_t P, int32_t layout, int causal) {
+  auto pieces = rank_pieces(S, P, layout);
+  s.n_groups = 0;
+  s.n_segs = 0;
+  for (int r = 0; r < P; ++r)
+    for (const Piece& k : pieces[r]) {
+      add_group(s, k);
+      for (int r2 = 0; r2 < P; ++r2)
+        for (const Piece& q : pieces[r2])
+          if (maybe_visible(q, k, causal)) add_seg(s, q);
+    }
+  sort_groups_by_work(s);
+}
+
+int32_t resolve_layout(int32_t reorder, const int32_t* cu) {
+  if (reorder == CP_REORDER_AUTO) return cu ? CP_REORDER_STRIPED : CP_REORDER_DUAL_CHUNK_SWAP;
+  return reorder;
+}
+
+cp_status launch_fwd(const AttnArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
+                     int64_t k_rows, cudaStream_t st) {
+  (void)q_rows;
+  (void)k_rows;
+  return launch_attn_fwd_simt(a, s, dtype == CP_BF16, st);
+}
+
+cp_status launch_bwd(const BwdArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
+                     int64_t k_rows, cudaStream_t st) {
+  (void)q_rows;
+  (void)k_rows;
+  return launch_attn_bwd_simt(a, s, dtype == CP_BF16, st);
+}
+
+AttnArgs make_fwd_args(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int32_t Hq, int32_t Hkv, int32_t D, int64_t lse_ld, int32_t causal,
+                       const int32_t* cu, int32_t n_docs, float scale, int o_f32) {
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.q_ld = (int64_t)Hq * D;
+  a.k_ld = (int64_t)Hkv * D;
+  a.o_ld = (int64_t)Hq * D;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.lse_ld = (int32_t)lse_ld;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal;
+  a.cu_seqlens = cu;
+  a.n_docs = cu ? n_docs : 0;
+  a.err = device_error_word();
+  a.o_f32 = o_f32;
+  return a;
+}
+
+// ---------------------------------------------------------------- workspace layouts
+// Partial results of the STEPWISE ring (fp32), relative to their own base.
+struct RingPartialsWs {
+  size_t o_acc, lse_acc, o_step, lse_step, total;
+};
+RingPartialsWs ring_partials_ws(int64_t S, int32_t Hq, int32_t D, int32_t mode) {
+  RingPartialsWs w;
+  size_t off = 0;
+  w.o_acc = w.lse_acc = w.o_step = w.lse_step = 0;
+  if (mode == CP_RING_STEPWISE) {
+    w.o_acc = off; off += align_up((size_t)S * Hq * D * 4);
+    w.lse_acc = off; off += align_up((size_t)S * Hq * 4);
+    w.o_step = off; off += align_up((size_t)S * Hq * D * 4);
+    w.lse_step = off; off += align_up((size_t)S * Hq * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+struct RingFwdWs {
+  size_t q, k, v, o, lse, partials, total;
+  RingPartialsWs pw;
+};
+RingFwdWs ring_fwd_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t mode) {
+  RingFwdWs w;
+  size_t es = dtype_size(dtype);
+  size_t off = 0;
+  w.q = off; off += align_up((size_t)S * Hq * D * es);
+  w.k = off; off += align_up((size_t)S * Hkv * D * es);
+  w.v = off; off += align_up((size_t)S * Hkv * D * es);
+  w.o = off; off += align_up((size_t)S * Hq * D * es);
+  w.lse = off; off += align_up((size_t)S * Hq * 4);
+  w.pw = ring_partials_ws(S, Hq, D, mode);
+  w.partials = off; off += w.pw.total;
+  w.total = off;
+  return w;
+}
+
+struct RingBwdWs {
+  size_t q, k, v, o, dout, lse, delta, dq, dk, dv, total;
+};
+RingBwdWs ring_bwd_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype) {
+  RingBwdWs w;
+  size_t es = dtype_size(dtype);
+  size_t off = 0;
+  w.q = off; off += align_up((size_t)S * Hq * D * es);
+  w.k = off; off += align_up((size_t)S * Hkv * D * es);
+  w.v = off; off += align_up((size_t)S * Hkv * D * es);
+  w.o = off; off += align_up((size_t)S * Hq * D * es);
+  w.dout = off; off += align_up((size_t)S * Hq * D * es);
+  w.lse = off; off += align_up((size_t)S * Hq * 4);
+  w.delta = off; off += align_up((size_t)S * Hq * 4);
+  w.dq = off; off += align_up((size_t)S * Hq * D * 4);
+  w.dk = off; off += align_up((size_t)S * Hkv * D * 4);
+  w.dv = off; off += align_up((size_t)S * Hkv * D * 4);
+  w.total = off;
+  return w;
+}
+
+struct BlockBwdWs {
+  size_t delta, dq, dk, dv, total;
+};
+BlockBwdWs block_bwd_ws(int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t D) {
+  BlockBwdWs w;
+  size_t off = 0;
+  w.delta = off; off += align_up((size_t)Sq * Hq * 4);
+  w.dq = off; off += align_up((size_t)Sq * Hq * D * 4);
+  w.dk = off; off += align_up((size_t)Sk * Hkv * D * 4);
+  w.dv = off; off += align_up((size_t)Sk * Hkv * D * 4);
+  w.total = off;
+  return w;
+}
+
+struct UlyssesWs {
+  size_t q, k, v, o, total;
+};
+UlyssesWs ulysses_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype) {
+  UlyssesWs w;
+  size_t es = dtype_size(dtype);
+  size_t off = 0;
+  w.q = off; off += align_up((size_t)S * Hq * D * es);
+  w.k = off; off += align_up((size_t)S * Hkv * D * es);
+  w.v = off; off += align_up((size_t)S * Hkv * D * es);
+  w.o = off; off += align_up((size_t)S * Hq * D * es);
+  w.total = off;
+  return w;
+}
+
+char* ws_at(void* base, size_t off) { return static_cast<char*>(base) + off; }
+
+// The ring over P virtual ranks on buffers already in the ranks' layout:
+// q/k/v/o rows in rank order, lse columns in rank order.
+cp_status ring_core(const void* q_re, const void* k_re, const void* v_re, void* o_re, float* lse_re,
+                    int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                    int32_t layout, int32_t mode, const int32_t* cu_seqlens, int32_t n_docs,
+                    void* partials, const RingPartialsWs& w, cudaStream_t st) {
+  const float scale = 1.0f / sqrtf((float)D);
+  Schedule* s = new Schedule;
+  cp_status result = CP_OK;
+  if (mode == CP_RING_FUSED) {
+    build_ring_schedule(*s, S, P, layout, -1, 1);
+    AttnArgs a = make_fwd_args(q_re, k_re, v_re, o_re, lse_re, Hq, Hkv, D, S, 1, cu_seqlens,
+                               n_docs, scale, 0);
+    result = launch_fwd(a, *s, dtype, S, S, st);
+  } else {
+    float* o_acc = reinterpret_cast<float*>(ws_at(partials, w.o_acc));
+    float* lse_acc = reinterpret_cast<float*>(ws_at(partials, w.lse_acc));
+    float* o_step = reinterpret_cast<float*>(ws_at(partials, w.o_step));
+    float* lse_step = reinterpret_cast<float*>(ws_at(partials, w.lse_step));
+    for (int step = 0; step < P && result == CP_OK; ++step) {
+      build_ring_schedule(*s, S, P, layout, step, 1);
+      float* o_dst = step == 0 ? o_acc : o_step;
+      float* l_dst = step == 0 ? lse_acc : lse_step;
+      AttnArgs a = make_fwd_args(q_re, k_re, v_re, o_dst, l_dst, Hq, Hkv, D, S, 1, cu_seqlens,
+                                 n_docs, scale, 1);
+      result = launch_fwd(a, *s, dtype, S, S, st);
+      if (result == CP_OK && step > 0)
+        result = launch_lse_merge(o_acc, lse_acc, o_step, lse_step, o_acc, lse_acc, S, Hq, D, 1, st);
+    }
+    if (result == CP_OK) result = launch_cast_out(o_acc, o_re, S * Hq * D, dtype == CP_BF16, st);
+    if (result == CP_OK)
+      result = cuda_check(cudaMemcpyAsync(lse_re, lse_acc, (size_t)S * Hq * 4,
+                                          cudaMemcpyDeviceToDevice, st), "lse copy");
+  }
+  delete s;
+  return result;
+}
+
+cp_status check_ring_args(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                          int32_t layout, const int32_t* cu, int32_t n_docs) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(P >= 1 && P <= 32, CP_ERR_INVALID_ARG, "P must be in [1, 32]");
+  CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
+  CP_REQUIRE(layout >= CP_REORDER_CONTIGUOUS && layout <= CP_REORDER_STRIPED, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  if (layout == CP_REORDER_DUAL_CHUNK_SWAP) {
+    CP_REQUIRE(S % (2 * P) == 0, CP_ERR_SHAPE, "DUAL_CHUNK_SWAP needs S % (2P) == 0");
+    CP_REQUIRE(P <= 16, CP_ERR_UNSUPPORTED, "DUAL_CHUNK_SWAP supports P <= 16");
+  } else {
+    CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "ring needs S % P == 0");
+  }
+  CP_REQUIRE(S * (int64_t)Hq < (int64_t)INT32_MAX, CP_ERR_UNSUPPORTED, "S*Hq must be < 2^31");
+  if (cu) {
+    CP_REQUIRE(layout != CP_REORDER_CONTIGUOUS, CP_ERR_UNSUPPORTED,
+               "packed documents are supported only with a load-balanced ring "
+               "(DUAL_CHUNK_SWAP, STRIPED or AUTO)");
+    CP_REQUIRE(n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  }
+  return CP_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* cp_version(void) { return "0.1.0"; }
+
+const char* cp_last_error(void) { return g_last_error.c_str(); }
+
+const char* cp_status_string(int32_t st) {
+  switch (st) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG";
+    case CP_ERR_SHAPE: return "CP_ERR_SHAPE";
+    case CP_ERR_DTYPE: return "CP_ERR_DTYPE";
+    case CP_ERR_ALIGN: return "CP_ERR_ALIGN";
+    case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED";
+    case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA";
+    case CP_ERR_DEVICE_TIMEOUT: return "CP_ERR_DEVICE_TIMEOUT";
+    default: return "CP_ERR_UNKNOWN";
+  }
+}
+
+cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t Sq, int64_t Sk,
+                            int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask,
+                            float scale, void* out, float* lse, void* stream) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
+  CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
+             CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
+  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0};
+  if (mask) m = *mask;
+  CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
+                 fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
+                 fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
+             CP_ERR_UNSUPPORTED, "positions must fit in int32");
+  CP_REQUIRE(!m.cu_seqlens || m.n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  if (Sq == 0) return CP_OK;
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", Sk == 0);
+  CP_CHECK_T(v, "v", Sk == 0);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  if (scale == 0.f) scale = 1.0f / sqrtf((float)D);
+  Schedule* s = new Schedule;
+  s->n_groups = 0;
+  s->n_segs = 0;
+  add_group(*s, Piece{0, (int32_t)Sq, (int32_t)m.q_offset, (int32_t)m.q_stride});
+  s->g[0].lse_col0 = 0;
+  if (Sk > 0) add_seg(*s, Piece{0, (int32_t)Sk, (int32_t)m.k_offset, (int32_t)m.k_stride});
+  AttnArgs a = make_fwd_args(q, k, v, out, lse, Hq, Hkv, D, Sq, m.causal, m.cu_seqlens, m.n_docs,
+                             scale, 0);
+  cp_status st = launch_fwd(a, *s, dtype, Sq, Sk, (cudaStream_t)stream);
+  delete s;
+  return st;
+}
+
+cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
+                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
+  CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
+             CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
+  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0};
+  if (mask) m = *mask;
+  CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
+                 fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
+                 fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
+             CP_ERR_UNSUPPORTED, "positions must fit in int32");
+  CP_REQUIRE(!m.cu_seqlens || m.n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  if (Sq == 0 && Sk == 0) return CP_OK;
+  BlockBwdWs w = block_bwd_ws(Sq, Sk, Hq, Hkv, D);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for block bwd");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", Sq == 0);
+  CP_CHECK_T(out, "out", Sq == 0);
+  CP_CHECK_T(dout, "dout", Sq == 0);
+  CP_CHECK_T(lse, "lse", Sq == 0);
+  CP_CHECK_T(dq, "dq", Sq == 0);
+  CP_CHECK_T(k, "k", Sk == 0);
+  CP_CHECK_T(v, "v", Sk == 0);
+  CP_CHECK_T(dk, "dk", Sk == 0);
+  CP_CHECK_T(dv, "dv", Sk == 0);
+  if (scale == 0.f) scale = 1.0f / sqrtf((float)D);
+  cudaStream_t st = (cudaStream_t)stream;
+  float* delta = reinterpret_cast<float*>(ws_at(workspace, w.delta));
+  float* dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
+  float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
+  float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
+  const int is_bf16 = dtype == CP_BF16;
+  CP_TRY(launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, st));
+  CP_TRY(launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, st));
+  CP_TRY(launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, st));
+  CP_TRY(launch_bwd_preprocess(out, dout, delta, Sq, Hq, D, (int32_t)Sq, is_bf16, st));
+  Schedule* s = new Schedule;
+  s->n_groups = 0;
+  s->n_segs = 0;
+  add_group(*s, Piece{0, (int32_t)Sk, (int32_t)m.k_offset, (int32_t)m.k_stride});
+  if (Sq > 0) add_seg(*s, Piece{0, (int32_t)Sq, (int32_t)m.q_offset, (int32_t)m.q_stride});
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
+  a.dq_acc = dq_acc; a.dk_acc = dk_acc; a.dv_acc = dv_acc;
+  a.q_ld = (int64_t)Hq * D; a.k_ld = (int64_t)Hkv * D;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)Sq;
+  a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
+  a.err = device_error_word();
+  cp_status stt = launch_bwd(a, *s, dtype, Sq, Sk, st);
+  delete s;
+  CP_TRY(stt);
+  CP_TRY(launch_cast_out(dq_acc, dq, Sq * Hq * D, is_bf16, st));
+  CP_TRY(launch_cast_out(dk_acc, dk, Sk * Hkv * D, is_bf16, st));
+  CP_TRY(launch_cast_out(dv_acc, dv, Sk * Hkv * D, is_bf16, st));
+  return CP_OK;
+}
+
+cp_status cp_lse_merge(const void* o1, const float* lse1, const void* o2, const float* lse2,
+                       void* o, float* lse, int64_t Sq, int32_t H, int32_t D, int32_t o_dtype,
+                       void* stream) {
+  CP_REQUIRE(o_dtype == CP_F32 || o_dtype == CP_BF16, CP_ERR_DTYPE, "o_dtype must be CP_F32 or CP_BF16");
+  CP_REQUIRE(Sq >= 0 && H >= 1 && D >= 1, CP_ERR_INVALID_ARG, "Sq >= 0, H >= 1, D >= 1 required");
+  CP_REQUIRE(((size_t)D * dtype_size(o_dtype)) % 16 == 0, CP_ERR_ALIGN,
+             "D * sizeof(o_dtype) must be a multiple of 16 bytes");
+  CP_REQUIRE((size_t)D * dtype_size(o_dtype) <= 512, CP_ERR_UNSUPPORTED,
+             "D * sizeof(o_dtype) must be <= 512 bytes");
+  if (Sq == 0) return CP_OK;
+  CP_CHECK_T(o1, "o1", false);
+  CP_CHECK_T(o2, "o2", false);
+  CP_CHECK_T(o, "o", false);
+  CP_REQUIRE(lse1 && lse2 && lse, CP_ERR_INVALID_ARG, "lse pointers must not be NULL");
+  return launch_lse_merge(o1, lse1, o2, lse2, o, lse, Sq, H, D, o_dtype == CP_F32,
+                          (cudaStream_t)stream);
+}
+
+static cp_status permute_common(int kind, const void* x, void* y, int64_t S, int32_t H, int32_t D,
+                                int32_t P, int32_t dtype, void* stream) {
+  CP_REQUIRE(dtype == CP_F32 || dtype == CP_BF16, CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  CP_REQUIRE(S >= 0 && H >= 1 && D >= 1, CP_ERR_INVALID_ARG, "S >= 0, H >= 1, D >= 1 required");
+  CP_REQUIRE(P >= 1 && P <= 1024, CP_ERR_INVALID_ARG, "P must be in [1, 1024]");
+  size_t row_bytes = (size_t)H * D * dtype_size(dtype);
+  if (kind == kSeq2Head || kind == kHead2Seq) {
+    CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "Ulysses needs S % P == 0");
+    CP_REQUIRE(H % P == 0, CP_ERR_SHAPE, "Ulysses needs H % P == 0 (degree limited by heads)");
+    CP_REQUIRE((row_bytes / P) % 16 == 0, CP_ERR_ALIGN,
+               "(H/P)*D*sizeof(dtype) must be a multiple of 16 bytes");
+    CP_REQUIRE((uint64_t)S * P < (1ull << 32), CP_ERR_UNSUPPORTED, "S*P must be < 2^32");
+  } else if (kind == kZigzagReorder || kind == kZigzagRestore) {
+    CP_REQUIRE(S % (2 * P) == 0, CP_ERR_SHAPE, "zigzag needs S % (2P) == 0");
+    CP_REQUIRE(row_bytes % 16 == 0, CP_ERR_ALIGN, "H*D*sizeof(dtype) must be a multiple of 16 bytes");
+  } else {
+    CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "striped needs S % P == 0");
+    CP_REQUIRE(row_bytes % 16 == 0, CP_ERR_ALIGN, "H*D*sizeof(dtype) must be a multiple of 16 bytes");
+  }
+  if (S == 0) return CP_OK;
+  CP_CHECK_T(x, "x", false);
+  CP_CHECK_T(y, "y", false);
+  const char* xb = static_cast<const char*>(x);
+  const char* yb = static_cast<const char*>(y);
+  size_t nbytes = (size_t)S * row_bytes;
+  CP_REQUIRE(xb + nbytes <= yb || yb + nbytes <= xb, CP_ERR_INVALID_ARG, "x and y must not overlap");
+  return launch_row_gather(kind, x, y, S, (int64_t)row_bytes, P, H, (cudaStream_t)stream);
+}
+
+cp_status cp_ulysses_seq2head(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                              int32_t dtype, void* stream) {
+  return permute_common(kSeq2Head, x, y, S, H, D, P, dtype, stream);
+}
+cp_status cp_ulysses_head2seq(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                              int32_t dtype, void* stream) {
+  return permute_common(kHead2Seq, y, x, S, H, D, P, dtype, stream);
+}
+cp_status cp_zigzag_reorder(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                            int32_t dtype, void* stream) {
+  return permute_common(kZigzagReorder, x, y, S, H, D, P, dtype, stream);
+}
+cp_status cp_zigzag_restore(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                            int32_t dtype, void* stream) {
+  return permute_common(kZigzagRestore, y, x, S, H, D, P, dtype, stream);
+}
+cp_status cp_striped_reorder(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                             int32_t dtype, void* stream) {
+  return permute_common(kStripedReorder, x, y, S, H, D, P, dtype, stream);
+}
+cp_status cp_striped_restore(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                             int32_t dtype, void* stream) {
+  return permute_common(kStripedRestore, y, x, S, H, D, P, dtype, stream);
+}
+
+cp_status cp_lse_reorder(const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                         int32_t reorder, int32_t inverse, void* stream) {
+  CP_REQUIRE(reorder == CP_REORDER_DUAL_CHUNK_SWAP || reorder == CP_REORDER_STRIPED,
+             CP_ERR_INVALID_ARG, "reorder must be DUAL_CHUNK_SWAP or STRIPED");
+  CP_REQUIRE(S >= 0 && H >= 1 && P >= 1 && P <= 1024, CP_ERR_INVALID_ARG, "bad sizes");
+  CP_REQUIRE(S % (reorder == CP_REORDER_DUAL_CHUNK_SWAP ? 2 * P : P) == 0, CP_ERR_SHAPE,
+             "S must divide into the layout's chunks");
+  CP_REQUIRE((uint64_t)S * H < (1ull << 32), CP_ERR_UNSUPPORTED, "S*H must be < 2^32");
+  if (S == 0) return CP_OK;
+  CP_REQUIRE(x && y, CP_ERR_INVALID_ARG, "x and y must not be NULL");
+  CP_REQUIRE(x + (size_t)S * H <= y || y + (size_t)S * H <= x, CP_ERR_INVALID_ARG,
+             "x and y must not overlap");
+  int kind = reorder == CP_REORDER_DUAL_CHUNK_SWAP ? (inverse ? kZigzagRestore : kZigzagReorder)
+                                                   : (inverse ? kStripedRestore : kStripedReorder);
+  return launch_lse_permute(kind, x, y, S, H, P, (cudaStream_t)stream);
+}
+
+cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                            int32_t dtype, int32_t P, int32_t mode, size_t* bytes) {
+  CP_REQUIRE(bytes != nullptr, CP_ERR_INVALID_ARG, "bytes must not be NULL");
+  CP_REQUIRE(S >= 0 && Hq >= 1 && Hkv >= 1 && D >= 1 && P >= 1, CP_ERR_INVALID_ARG,
+             "sizes must be positive");
+  CP_REQUIRE(dtype == CP_F32 || dtype == CP_BF16, CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  switch (op) {
+    case CP_OP_RING_FWD:
+      CP_REQUIRE(mode == CP_RING_FUSED || mode == CP_RING_STEPWISE, CP_ERR_INVALID_ARG,
+                 "mode must be a cp_ring_mode value");
+      *bytes = ring_fwd_ws(S, Hq, Hkv, D, dtype, mode).total;
+      return CP_OK;
+    case CP_OP_RING_BWD:
+      *bytes = ring_bwd_ws(S, Hq, Hkv, D, dtype).total;
+      return CP_OK;
+    case CP_OP_ULYSSES_FWD:
+      *bytes = ulysses_ws(S, Hq, Hkv, D, dtype).total;
+      return CP_OK;
+    case CP_OP_BLOCK_BWD:  // S is max(Sq, Sk) here
+      *bytes = block_bwd_ws(S, S, Hq, Hkv, D).total;
+      return CP_OK;
+    case CP_OP_RING_FWD_REORDERED:
+      CP_REQUIRE(mode == CP_RING_FUSED || mode == CP_RING_STEPWISE, CP_ERR_INVALID_ARG,
+                 "mode must be a cp_ring_mode value");
+      *bytes = ring_partials_ws(S, Hq, D, mode).total;
+      return CP_OK;
+    default:
+      set_last_error("op must be a cp_op value");
+      return CP_ERR_INVALID_ARG;
+  }
+}
+
+cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                            int32_t mode, const int32_t* cu_seqlens, int32_t n_docs, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  CP_REQUIRE(reorder >= CP_REORDER_CONTIGUOUS && reorder <= CP_REORDER_AUTO, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  CP_REQUIRE(mode == CP_RING_FUSED || mode == CP_RING_STEPWISE, CP_ERR_INVALID_ARG,
+             "mode must be a cp_ring_mode value");
+  int32_t layout = resolve_layout(reorder, cu_seqlens);
+  CP_TRY(check_ring_args(S, Hq, Hkv, D, dtype, P, layout, cu_seqlens, n_docs));
+  if (S == 0) return CP_OK;
+  RingFwdWs w = ring_fwd_ws(S, Hq, Hkv, D, dtype, mode);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for ring fwd");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t es = dtype_size(dtype);
+  void* q_re = ws_at(workspace, w.q);
+  void* k_re = ws_at(workspace, w.k);
+  void* v_re = ws_at(workspace, w.v);
+  void* o_re = ws_at(workspace, w.o);
+  float* lse_re = reinterpret_cast<float*>(ws_at(workspace, w.lse));
+  const int fwd_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagReorder : kStripedReorder;
+  const int back_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagRestore : kStripedRestore;
+  // Contiguous layout: rank r already holds rows [rC, (r+1)C) in place.
+  const bool moved = layout != CP_REORDER_CONTIGUOUS;
+  if (moved) {
+    CP_TRY(launch_row_gather(fwd_kind, q, q_re, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_row_gather(fwd_kind, k, k_re, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(fwd_kind, v, v_re, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  } else {
+    q_re = const_cast<void*>(q);
+    k_re = const_cast<void*>(k);
+    v_re = const_cast<void*>(v);
+    o_re = out;
+    lse_re = lse;
+  }
+  CP_TRY(ring_core(q_re, k_re, v_re, o_re, lse_re, S, Hq, Hkv, D, dtype, P, layout, mode,
+                   cu_seqlens, n_docs, ws_at(workspace, w.partials), w.pw, st));
+  if (moved) {
+    CP_TRY(launch_row_gather(back_kind, o_re, out, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_lse_permute(back_kind, lse_re, lse, S, Hq, P, st));
+  }
+  return CP_OK;
+}
+
+cp_status cp_ring_attention_reordered(const void* q, const void* k, const void* v, int64_t S,
+                                      int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                                      int32_t reorder, int32_t mode, const int32_t* cu_seqlens,
+                                      int32_t n_docs, void* out, float* lse, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  CP_REQUIRE(reorder >= CP_REORDER_CONTIGUOUS && reorder <= CP_REORDER_AUTO, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  CP_REQUIRE(mode == CP_RING_FUSED || mode == CP_RING_STEPWISE, CP_ERR_INVALID_ARG,
+             "mode must be a cp_ring_mode value");
+  int32_t layout = resolve_layout(reorder, cu_seqlens);
+  CP_TRY(check_ring_args(S, Hq, Hkv, D, dtype, P, layout, cu_seqlens, n_docs));
+  if (S == 0) return CP_OK;
+  RingPartialsWs w = ring_partials_ws(S, Hq, D, mode);
+  if (w.total > 0) {
+    CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE,
+               "workspace too small for the stepwise ring");
+    CP_CHECK_T(workspace, "workspace", false);
+  }
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  return ring_core(q, k, v, out, lse, S, Hq, Hkv, D, dtype, P, layout, mode, cu_seqlens, n_docs,
+                   workspace, w, (cudaStream_t)stream);
+}
+
+cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, int64_t S, int32_t Hq,
+                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                                const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
+                                void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  CP_REQUIRE(reorder >= CP_REORDER_CONTIGUOUS && reorder <= CP_REORDER_AUTO, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  int32_t layout = resolve_layout(reorder, cu_seqlens);
+  CP_TRY(check_ring_args(S, Hq, Hkv, D, dtype, P, layout, cu_seqlens, n_docs));
+  if (S == 0) return CP_OK;
+  RingBwdWs w = ring_bwd_ws(S, Hq, Hkv, D, dtype);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for ring bwd");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(dout, "dout", false);
+  CP_CHECK_T(dq, "dq", false);
+  CP_CHECK_T(dk, "dk", false);
+  CP_CHECK_T(dv, "dv", false);
+  CP_REQUIRE(lse != nullptr, CP_ERR_INVALID_ARG, "lse must not be NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t es = dtype_size(dtype);
+  const int is_bf16 = dtype == CP_BF16;
+  const bool moved = layout != CP_REORDER_CONTIGUOUS;
+  const int fwd_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagReorder : kStripedReorder;
+  const int back_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagRestore : kStripedRestore;
+  const void *q_re = q, *k_re = k, *v_re = v, *o_re = out, *do_re = dout;
+  const float* lse_re = lse;
+  if (moved) {
+    void* qw = ws_at(workspace, w.q);
+    void* kw = ws_at(workspace, w.k);
+    void* vw = ws_at(workspace, w.v);
+    void* ow = ws_at(workspace, w.o);
+    void* dw = ws_at(workspace, w.dout);
+    float* lw = reinterpret_cast<float*>(ws_at(workspace, w.lse));
+    CP_TRY(launch_row_gather(fwd_kind, q, qw, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_row_gather(fwd_kind, k, kw, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(fwd_kind, v, vw, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(fwd_kind, out, ow, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_row_gather(fwd_kind, dout, dw, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_lse_permute(fwd_kind, lse, lw, S, Hq, P, st));
+    q_re = qw; k_re = kw; v_re = vw; o_re = ow; do_re = dw; lse_re = lw;
+  }
+  float* delta = reinterpret_cast<float*>(ws_at(workspace, w.delta));
+  float* dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
+  float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
+  float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
+  CP_TRY(launch_zero(dq_acc, (size_t)S * Hq * D * 4, st));
+  CP_TRY(launch_bwd_preprocess(o_re, do_re, delta, S, Hq, D, (int32_t)S, is_bf16, st));
+  Schedule* s = new Schedule;
+  build_ring_bwd_schedule(*s, S, P, layout, 1);
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q_re; a.k = k_re; a.v = v_re; a.dout = do_re; a.lse = lse_re; a.delta = delta;
+  a.dq_acc = dq_acc; a.dk_acc = dk_acc; a.dv_acc = dv_acc;
+  a.q_ld = (int64_t)Hq * D; a.k_ld = (int64_t)Hkv * D;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)S;
+  a.scale = 1.0f / sqrtf((float)D);
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.causal = 1; a.cu_seqlens = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0;
+  a.err = device_error_word();
+  cp_status stt = launch_bwd(a, *s, dtype, S, S, st);
+  delete s;
+  CP_TRY(stt);
+  if (moved) {
+    // q/k/v staging buffers are free now: cast into them, then restore the order.
+    void* dq_c = ws_at(workspace, w.q);
+    void* dk_c = ws_at(workspace, w.k);
+    void* dv_c = ws_at(workspace, w.v);
+    CP_TRY(launch_cast_out(dq_acc, dq_c, S * Hq * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dk_acc, dk_c, S * Hkv * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dv_acc, dv_c, S * Hkv * D, is_bf16, st));
+    CP_TRY(launch_row_gather(back_kind, dq_c, dq, S, (int64_t)Hq * D * es, P, Hq, st));
+    CP_TRY(launch_row_gather(back_kind, dk_c, dk, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(back_kind, dv_c, dv, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  } else {
+    CP_TRY(launch_cast_out(dq_acc, dq, S * Hq * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dk_acc, dk, S * Hkv * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dv_acc, dv, S * Hkv * D, is_bf16, st));
+  }
+  return CP_OK;
+}
+
+cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                               int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                               const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(P >= 1 && P <= 64, CP_ERR_INVALID_ARG, "P must be in [1, 64]");
+  CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
+  CP_REQUIRE(Hq % P == 0 && Hkv % P == 0, CP_ERR_SHAPE,
+             "Ulysses needs Hq % P == 0 and Hkv % P == 0 (degree limited by the key/value heads)");
+  CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "Ulysses needs S % P == 0");
+  CP_REQUIRE(S * (int64_t)Hq < (int64_t)INT32_MAX && S * (int64_t)P < (int64_t)INT32_MAX,
+             CP_ERR_UNSUPPORTED, "S*Hq and S*P must be < 2^31");
+  CP_REQUIRE(!cu_seqlens || n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  const size_t es = dtype_size(dtype);
+  CP_REQUIRE(((size_t)(Hkv / P) * D * es) % 16 == 0, CP_ERR_ALIGN,
+             "(Hkv/P)*D*sizeof(dtype) must be a multiple of 16 bytes");
+  if (S == 0) return CP_OK;
+  UlyssesWs w = ulysses_ws(S, Hq, Hkv, D, dtype);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for Ulysses");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  cudaStream_t st = (cudaStream_t)stream;
+  void* qh = ws_at(workspace, w.q);
+  void* kh = ws_at(workspace, w.k);
+  void* vh = ws_at(workspace, w.v);
+  void* oh = ws_at(workspace, w.o);
+  CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
+  CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  const int32_t Hqp = Hq / P, Hkvp = Hkv / P;
+  Schedule* s = new Schedule;
+  s->n_groups = 0;
+  s->n_segs = 0;
+  for (int p = 0; p < P; ++p) {
+    add_group(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
+    s->g[p].lse_col0 = 0;
+    s->g[p].lse_head0 = p * Hqp;
+    add_seg(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
+  }
+  AttnArgs a = make_fwd_args(qh, kh, vh, oh, lse, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
+                             1.0f / sqrtf((float)D), 0);
+  cp_status stt = launch_fwd(a, *s, dtype, (int64_t)P * S, (int64_t)P * S, st);
+  delete s;
+  CP_TRY(stt);
+  CP_TRY(launch_row_gather(kHead2Seq, oh, out, S, (int64_t)Hq * D * es, P, Hq, st));
+  return CP_OK;
+}
+
+cp_status cp_check_device_status(void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  cp_status s = cuda_check(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  if (s != CP_OK) return s;
+  int32_t* ew = device_error_word();
+  if (!ew) {
+    set_last_error("device error word unavailable");
+    return CP_ERR_CUDA;
+  }
+  int32_t code = 0;
+  s = cuda_check(cudaMemcpy(&code, ew, sizeof(code), cudaMemcpyDeviceToHost), "read error word");
+  if (s != CP_OK) return s;
+  if (code != 0) {
+    int32_t zero = 0;
+    (void)cudaMemcpy(ew, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    set_last_error("a kernel gave up on a bounded wait (device error code " +
+                   std::to_string(code) + ")");
+    return CP_ERR_DEVICE_TIMEOUT;
+  }
+  return CP_OK;
+}
+
+cp_status cp_debug_bounded_wait(int32_t timeout_us, void* stream) {
+  CP_REQUIRE(timeout_us >= 1 && timeout_us <= 1000000, CP_ERR_INVALID_ARG,
+             "timeout_us must be in [1, 1000000]");
+  int32_t* ew = device_error_word();
+  CP_REQUIRE(ew != nullptr, CP_ERR_CUDA, "device error word unavailable");
+  return launch_bounded_wait_probe(timeout_us, ew, (cudaStream_t)stream);
+}
+
+}  // extern "C"

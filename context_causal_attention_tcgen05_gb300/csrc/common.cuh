@@ -1,0 +1,220 @@
+// Internal declarations shared by the library's translation units.
+//
+// The attention kernels consume a "schedule": a list of query groups, each
+// with the list of key/value segments it attends to, in the order the ring
+// visits them.  One schedule describes every use of block attention in the
+// library: a single block pair (one group, one segment), the P virtual ranks
+// of the ring (a group per query chunk, segments in ring order), and the P
+// virtual ranks of Ulysses (a group per rank over the permuted buffer).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "cp_attn.h"
+
+namespace cpa {
+
+constexpr int kMaxGroups = 64;
+constexpr int kMaxSegs = 1024;
+
+// A run of query rows that share one affine position map.
+struct QGroup {
+  int32_t q_row0;      // first row in the q (and o) buffer
+  int32_t nq;          // number of rows
+  int32_t pos_off;     // global position of row 0
+  int32_t pos_stride;  // position step between rows (>= 1)
+  int32_t seg_begin;   // first segment index in Schedule::s
+  int32_t seg_count;   // number of segments
+  int32_t tile0;       // running count of query tiles before this group (set by the launcher)
+  int32_t lse_col0;    // lse column of row 0
+  int32_t lse_head0;   // lse head (row of the [H, cols] lse) of head 0
+  int32_t o_row0;      // first output row
+  int32_t pad0, pad1;
+};
+
+// A run of key/value rows with one affine position map.
+struct KSeg {
+  int32_t k_row0;
+  int32_t nk;
+  int32_t pos_off;
+  int32_t pos_stride;
+};
+
+struct Schedule {
+  int32_t n_groups;
+  int32_t n_segs;
+  QGroup g[kMaxGroups];
+  KSeg s[kMaxSegs];
+};
+
+// Everything else an attention launch needs (pointers, strides, mask).
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int64_t q_ld;  // elements between consecutive rows of q (Hq*D)
+  int64_t k_ld;  // elements between consecutive rows of k and v (Hkv*D)
+  int64_t o_ld;  // elements between consecutive rows of o
+  int32_t Hq, Hkv, D;
+  int32_t lse_ld;     // columns per lse head row
+  float scale_log2;   // softmax scale * log2(e)
+  float scale;        // softmax scale
+  int32_t causal;
+  const int32_t* cu_seqlens;  // device, n_docs+1, or nullptr
+  int32_t n_docs;
+  int32_t* err;       // device error word
+  int32_t total_units;
+  int32_t o_f32;      // output dtype: 1 fp32, 0 same as input
+};
+
+// Backward extras.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const float* lse;    // [Hq, lse_ld], natural log
+  const float* delta;  // [Hq, lse_ld], rowsum(dout*out)
+  float* dq_acc;       // [rows_q, Hq, D] fp32
+  float* dk_acc;       // [rows_k, Hkv, D] fp32
+  float* dv_acc;       // [rows_k, Hkv, D] fp32
+  int64_t q_ld, k_ld;
+  int32_t Hq, Hkv, D;
+  int32_t lse_ld;
+  float scale_log2, scale;
+  int32_t causal;
+  const int32_t* cu_seqlens;
+  int32_t n_docs;
+  int32_t* err;
+  int32_t total_units;
+};
+
+// Device error codes written into the error word (first writer wins).
+enum DeviceError : int32_t {
+  kDevOk = 0,
+  kDevTimeout = 1,
+};
+
+// ---------------------------------------------------------------- host side helpers (api.cu)
+void set_last_error(const std::string& msg);
+int32_t* device_error_word();  // device address of the error word for the current device
+cp_status cuda_check(cudaError_t e, const char* what);
+
+// ---------------------------------------------------------------- launchers (one per .cu)
+// movers.cu
+cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t row_bytes,
+                            int32_t P, int32_t H_for_ulysses, cudaStream_t st);
+cp_status launch_lse_permute(int kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                             cudaStream_t st);
+// merge.cu
+cp_status launch_lse_merge(const void* o1, const float* lse1, const void* o2, const float* lse2,
+                           void* o, float* lse, int64_t Sq, int32_t H, int32_t D, int32_t o_f32,
+                           cudaStream_t st);
+// attn_simt.cu
+cp_status launch_attn_fwd_simt(const AttnArgs& a, Schedule& s, int is_bf16, cudaStream_t st);
+cp_status launch_attn_bwd_simt(const BwdArgs& a, Schedule& s, int is_bf16, cudaStream_t st);
+cp_status launch_bwd_preprocess(const void* out, const void* dout, float* delta, int64_t rows,
+                                int32_t H, int32_t D, int32_t lse_ld, int is_bf16, cudaStream_t st);
+cp_status launch_cast_out(const float* src, void* dst, int64_t n, int is_bf16, cudaStream_t st);
+cp_status launch_zero(void* p, size_t bytes, cudaStream_t st);
+cp_status launch_bounded_wait_probe(int32_t timeout_us, int32_t* err, cudaStream_t st);
+// attn_fwd_tc.cu
+cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
+                             cudaStream_t st);
+// attn_bwd_tc.cu
+cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
+                             cudaStream_t st);
+
+// Row-gather kinds.
+enum GatherKind : int {
+  kZigzagReorder = 0,
+  kZigzagRestore = 1,
+  kStripedReorder = 2,
+  kStripedRestore = 3,
+  kSeq2Head = 4,
+  kHead2Seq = 5,
+};
+
+// Fills group tile prefix sums for a query tile height; returns total units (tiles x heads).
+int64_t schedule_units(Schedule& s, int tile_rows, int heads);
+
+}  // namespace cpa
+
+// ---------------------------------------------------------------- device helpers
+namespace cpa {
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void record_device_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ float load_as_f32(const T* p);
+template <>
+__device__ __forceinline__ float load_as_f32<float>(const float* p) {
+  return *p;
+}
+template <>
+__device__ __forceinline__ float load_as_f32<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_from_f32(T* p, float x);
+template <>
+__device__ __forceinline__ void store_from_f32<float>(float* p, float x) {
+  *p = x;
+}
+template <>
+__device__ __forceinline__ void store_from_f32<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+// floor(a / b) for b > 0.
+__device__ __forceinline__ int64_t floor_div(int64_t a, int64_t b) {
+  int64_t q = a / b;
+  if ((a % b != 0) && (a < 0)) --q;
+  return q;
+}
+
+// Start and end (exclusive) of the packed document holding position p.
+__device__ __forceinline__ void doc_bounds(const int32_t* cu, int32_t n_docs, int64_t p,
+                                           int64_t* start, int64_t* end) {
+  int lo = 0, hi = n_docs - 1;
+  while (lo < hi) {  // largest d with cu[d] <= p
+    int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)__ldg(cu + mid) <= p) lo = mid; else hi = mid - 1;
+  }
+  *start = __ldg(cu + lo);
+  *end = __ldg(cu + lo + 1);
+}
+
+// Locates unit u in a schedule: query group, query tile index, head.
+__device__ __forceinline__ void decode_unit(const Schedule& s, int tile_rows, int heads, int u,
+                                            int* g_out, int* tile_out, int* h_out) {
+  int h = u % heads;
+  int rest = u / heads;
+  int g = 0;
+  for (int i = 1; i < s.n_groups; ++i)
+    if (s.g[i].tile0 <= rest) g = i;
+  int ntiles = (s.g[g].nq + tile_rows - 1) / tile_rows;
+  int local = rest - s.g[g].tile0;
+  *g_out = g;
+  *tile_out = ntiles - 1 - local;  // heaviest (last) tiles of a group first
+  *h_out = h;
+}
+
+}  // namespace cpa

@@ -1,0 +1,182 @@
+// Data-movement kernels of the hot path: the zigzag (DUAL_CHUNK_SWAP) and
+// striped reorders and their inverses, and the Ulysses sequence<->head
+// exchange, which on one GPU is a layout permute rather than an all-to-all.
+//
+// Sources: handbook chapter "Context parallelism: Ring Attention and Ulysses",
+// sections "Ulysses: transposing between the sequence and the heads"
+// (seq_to_head / head_to_seq) and "The zigzag partition" (rank r holds blocks
+// r and 2P-1-r of 2P); MaxText pull request "Add Packing Support for Context
+// Parallelism (Ring Attention) #2906" (ReorderStrategy STRIPED, read as
+// token-granular round robin: rank r holds positions r, r+P, ...).
+//
+// Every one of these is a gather of contiguous byte runs: output run u comes
+// from input run map(u).  Runs are multiples of 16 bytes, so each thread moves
+// 16-byte vectors; consecutive threads cover consecutive output vectors, so
+// stores are fully coalesced and loads are coalesced within a run (runs are
+// >= 512 bytes at the model shapes).  Loads and stores bypass L1 and are
+// marked streaming: every byte is touched exactly once.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace cpa {
+namespace {
+
+struct GatherParams {
+  const int4* x;
+  int4* y;
+  uint32_t total_vec;  // output vectors
+  uint32_t run_vec;    // vectors per run
+  uint32_t P;
+  uint32_t a;          // kind-specific: zigzag -> P; striped -> S/P; ulysses -> S
+  int kind;
+};
+
+__device__ __forceinline__ uint32_t source_run(const GatherParams& p, uint32_t u) {
+  switch (p.kind) {
+    case kZigzagReorder: {  // out run u = (rank r = u/2, half j = u%2) <- chunk j ? 2P-1-r : r
+      uint32_t r = u >> 1, j = u & 1;
+      return j ? (2 * p.P - 1 - r) : r;
+    }
+    case kZigzagRestore: {  // out run = chunk c <- (rank, half) slot
+      uint32_t c = u;
+      return c < p.P ? 2 * c : 2 * (2 * p.P - 1 - c) + 1;
+    }
+    case kStripedReorder: {  // out row u = r*(S/P) + i <- in row i*P + r
+      uint32_t r = u / p.a, i = u - r * p.a;
+      return i * p.P + r;
+    }
+    case kStripedRestore: {  // out row u = i*P + r <- in row r*(S/P) + i
+      uint32_t i = u / p.P, r = u - i * p.P;
+      return r * p.a + i;
+    }
+    case kSeq2Head: {  // out run u = rank p*S + s <- in run s*P + p  (run = H/P heads)
+      uint32_t rank = u / p.a, s = u - rank * p.a;
+      return s * p.P + rank;
+    }
+    default: {  // kHead2Seq: out run u = s*P + p <- in run p*S + s
+      uint32_t s = u / p.P, rank = u - s * p.P;
+      return rank * p.a + s;
+    }
+  }
+}
+
+constexpr int kThreads = 256;
+constexpr int kVecPerThread = 4;
+
+__global__ void __launch_bounds__(kThreads) row_gather_kernel(GatherParams p) {
+  uint32_t base = blockIdx.x * (kThreads * kVecPerThread) + threadIdx.x;
+  int4 buf[kVecPerThread];
+  uint32_t dst[kVecPerThread];
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    uint32_t i = base + k * kThreads;
+    dst[k] = i;
+    if (i < p.total_vec) {
+      uint32_t u = i / p.run_vec;
+      uint32_t w = i - u * p.run_vec;
+      uint64_t src = (uint64_t)source_run(p, u) * p.run_vec + w;
+      buf[k] = __ldcs(p.x + src);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k)
+    if (dst[k] < p.total_vec) __stcs(p.y + dst[k], buf[k]);
+}
+
+// lse [H, S] column permute with the row maps above (runs of one column).
+struct LsePermParams {
+  const float* x;
+  float* y;
+  uint32_t S, P, H, C;
+  int kind;
+};
+
+__device__ __forceinline__ uint32_t lse_source_col(const LsePermParams& p, uint32_t col) {
+  switch (p.kind) {
+    case kZigzagReorder: {  // col = r*2C + j*C + c
+      uint32_t r = col / (2 * p.C), rem = col - r * 2 * p.C, j = rem / p.C, c = rem - j * p.C;
+      uint32_t chunk = j ? (2 * p.P - 1 - r) : r;
+      return chunk * p.C + c;
+    }
+    case kZigzagRestore: {  // col = chunk*C + c
+      uint32_t chunk = col / p.C, c = col - chunk * p.C;
+      uint32_t slot = chunk < p.P ? 2 * chunk : 2 * (2 * p.P - 1 - chunk) + 1;
+      return slot * p.C + c;
+    }
+    case kStripedReorder: {  // col = r*(S/P) + i <- i*P + r
+      uint32_t n = p.S / p.P, r = col / n, i = col - r * n;
+      return i * p.P + r;
+    }
+    default: {  // kStripedRestore: col = i*P + r <- r*(S/P) + i
+      uint32_t n = p.S / p.P, i = col / p.P, r = col - i * p.P;
+      return r * n + i;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) lse_permute_kernel(LsePermParams p) {
+  uint64_t total = (uint64_t)p.S * p.H;
+  for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total; t += (uint64_t)gridDim.x * 256) {
+    uint32_t h = (uint32_t)(t / p.S), col = (uint32_t)(t - (uint64_t)h * p.S);
+    p.y[t] = p.x[(uint64_t)h * p.S + lse_source_col(p, col)];
+  }
+}
+
+}  // namespace
+
+cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t row_bytes,
+                            int32_t P, int32_t H_for_ulysses, cudaStream_t st) {
+  if (S == 0) return CP_OK;
+  GatherParams p;
+  p.x = static_cast<const int4*>(x);
+  p.y = static_cast<int4*>(y);
+  p.P = (uint32_t)P;
+  p.kind = kind;
+  uint64_t total_bytes = (uint64_t)S * (uint64_t)row_bytes;
+  uint64_t total_vec = total_bytes / 16;
+  if (total_vec >= (1ull << 32)) {
+    set_last_error("tensor larger than 64 GiB is not supported by the permute kernels");
+    return CP_ERR_UNSUPPORTED;
+  }
+  p.total_vec = (uint32_t)total_vec;
+  switch (kind) {
+    case kZigzagReorder:
+    case kZigzagRestore:
+      p.run_vec = (uint32_t)(total_vec / (2 * (uint64_t)P));
+      p.a = (uint32_t)P;
+      break;
+    case kStripedReorder:
+    case kStripedRestore:
+      p.run_vec = (uint32_t)(row_bytes / 16);
+      p.a = (uint32_t)(S / P);
+      break;
+    default:  // Ulysses: runs of H/P heads
+      p.run_vec = (uint32_t)(row_bytes / P / 16);  // (H/P)*D elements
+      p.a = (uint32_t)S;
+      break;
+  }
+  uint32_t per_block = kThreads * kVecPerThread;
+  uint32_t blocks = (p.total_vec + per_block - 1) / per_block;
+  row_gather_kernel<<<blocks, kThreads, 0, st>>>(p);
+  return cuda_check(cudaGetLastError(), "row_gather_kernel launch");
+}
+
+cp_status launch_lse_permute(int kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                             cudaStream_t st) {
+  if (S == 0 || H == 0) return CP_OK;
+  LsePermParams p;
+  p.x = x;
+  p.y = y;
+  p.S = (uint32_t)S;
+  p.P = (uint32_t)P;
+  p.H = (uint32_t)H;
+  p.C = (kind == kZigzagReorder || kind == kZigzagRestore) ? (uint32_t)(S / (2 * P)) : 0;
+  p.kind = kind;
+  uint64_t total = (uint64_t)S * H;
+  uint32_t blocks = (uint32_t)std::min<uint64_t>((total + 255) / 256, 152ull * 16);
+  lse_permute_kernel<<<blocks, 256, 0, st>>>(p);
+  return cuda_check(cudaGetLastError(), "lse_permute_kernel launch");
+}
+
+}  // namespace cpa

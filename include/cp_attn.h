@@ -1,0 +1,263 @@
+/*
+ * cp_attn.h -- C ABI of the GB300 (sm_103a) causal context-parallel attention library.
+ *
+ * The sequence of a causal softmax attention is split into P "virtual ranks"
+ * that all live in one GPU's HBM.  The calls below follow the statement of the
+ * problem in the handbook chapter "Context parallelism: Ring Attention and
+ * Ulysses" (sections "Which operations partition directly", "Ulysses:
+ * transposing between the sequence and the heads", "Ring Attention: passing
+ * the KV once around a ring", "The zigzag partition") and the reorder
+ * strategies of the MaxText pull request "Add Packing Support for Context
+ * Parallelism (Ring Attention) #2906" (ReorderStrategy DUAL_CHUNK_SWAP /
+ * STRIPED / AUTO).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are row-major [S, H, D] (D fastest) as in the handbook's
+ *    attention(q, k, v): q is [Sq, Hq, D], k and v are [Sk, Hkv, D].
+ *    Grouped-query attention: query head h reads key/value head h / (Hq/Hkv).
+ *  - lse (log-sum-exp of the scaled scores, natural log) is fp32 [H, Sq].
+ *  - Every tensor pointer is a DEVICE pointer, 16-byte aligned, owned by the
+ *    caller.  The library allocates no device memory: scratch space comes from
+ *    a caller workspace whose size cp_workspace_size() reports.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work and return; they do not synchronise,
+ *    except cp_check_device_status().
+ *  - Arguments are validated before any launch; a refused call launches
+ *    nothing and returns a negative cp_status; cp_last_error() then holds a
+ *    thread-local message naming the offending argument.
+ *  - dtype is CP_F32 or CP_BF16 for the q/k/v/out tensors; accumulation and
+ *    softmax are fp32 in both cases.  bf16 outputs are rounded to nearest even.
+ *  - A row that sees no key (all masked) has lse = -inf and out = 0.
+ */
+#ifndef CP_ATTN_H
+#define CP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CP_API __attribute__((visibility("default")))
+#else
+#define CP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1,    /* null pointer, bad enum, negative size */
+  CP_ERR_SHAPE = -2,          /* sizes that do not divide (S % P, H % P, Hq % Hkv, ...) */
+  CP_ERR_DTYPE = -3,          /* dtype not CP_F32 / CP_BF16, or not supported for this D */
+  CP_ERR_ALIGN = -4,          /* pointer not 16-byte aligned, row bytes not a multiple of 16 */
+  CP_ERR_UNSUPPORTED = -5,    /* valid in principle but not provided (e.g. packing with contiguous ring) */
+  CP_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than cp_workspace_size() */
+  CP_ERR_CUDA = -7,           /* a CUDA runtime call failed (launch error, ...) */
+  CP_ERR_DEVICE_TIMEOUT = -8  /* a kernel's bounded wait expired (reported by cp_check_device_status) */
+} cp_status;
+
+typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
+
+/* Load-balancing layout of the ring (ReorderStrategy of the MaxText packing PR).
+ * CONTIGUOUS: rank r holds positions [r*S/P, (r+1)*S/P).
+ * DUAL_CHUNK_SWAP (zigzag): 2P chunks of C = S/(2P); rank r holds chunk r then chunk 2P-1-r.
+ * STRIPED: rank r holds positions r, r+P, r+2P, ... (token-granular round robin).
+ * AUTO: STRIPED when documents are packed (cu_seqlens != NULL), else DUAL_CHUNK_SWAP. */
+typedef enum {
+  CP_REORDER_CONTIGUOUS = 0,
+  CP_REORDER_DUAL_CHUNK_SWAP = 1,
+  CP_REORDER_STRIPED = 2,
+  CP_REORDER_AUTO = 3
+} cp_reorder;
+
+/* How the ring's P steps are executed on one GPU.
+ * FUSED: one launch; each query tile walks the ring's key/value blocks in ring
+ *   order (src = r, r-1, ... mod P) and merges them in the kernel's online
+ *   softmax, which is the same log-sum-exp merge.
+ * STEPWISE: one attention launch per ring step writing a partial (o, lse) in
+ *   fp32, followed by cp_lse_merge into the running result, as in the ring
+ *   section's loop. */
+typedef enum { CP_RING_FUSED = 0, CP_RING_STEPWISE = 1 } cp_ring_mode;
+
+/* Which operation a workspace is sized for (cp_workspace_size). */
+typedef enum {
+  CP_OP_RING_FWD = 0,
+  CP_OP_RING_BWD = 1,
+  CP_OP_ULYSSES_FWD = 2,
+  CP_OP_BLOCK_BWD = 3,
+  CP_OP_RING_FWD_REORDERED = 4
+} cp_op;
+
+/* Visibility rule of one (query block, key block) pair.
+ * Query row i sits at global position q_offset + q_stride*i, key row j at
+ * k_offset + k_stride*j (strides >= 1; 1 = contiguous block, P = striped).
+ * causal != 0: key j is visible to query i only if pos_k(j) <= pos_q(i)
+ *   (the handbook's masked_fill(ki > qi) with offsets).
+ * cu_seqlens (DEVICE pointer, n_docs+1 int32 ascending from 0, or NULL):
+ *   packed documents; a key is visible only if it lies in the query's
+ *   document.  Positions must lie in [0, cu_seqlens[n_docs]). */
+typedef struct {
+  int32_t causal;
+  int64_t q_offset, k_offset;
+  int64_t q_stride, k_stride;
+  const int32_t* cu_seqlens;
+  int32_t n_docs;
+} cp_mask;
+
+/* ---------------------------------------------------------------- block attention */
+
+/* Forward attention of one block pair, returning out and the per-row lse
+ * ("Which operations partition directly": attention(q, k, v, causal,
+ * q_offset, k_offset) -> (out, lse)).
+ *   q [Sq,Hq,D], k/v [Sk,Hkv,D] in `dtype`; out [Sq,Hq,D] in `dtype`; lse [Hq,Sq] fp32.
+ *   mask: host pointer; NULL means causal with zero offsets, unit strides, one document.
+ *   scale: softmax scale; 0 means 1/sqrt(D).
+ * Supported: D in {16,32,64,128} for CP_F32 (FFMA kernel); D in {64,128} for
+ * CP_BF16 (tcgen05 kernel); Sq, Sk >= 0 (Sq = 0 is a no-op); Hq % Hkv == 0. */
+CP_API cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t Sq, int64_t Sk,
+                            int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask,
+                            float scale, void* out, float* lse, void* stream);
+
+/* Backward of cp_attn_block_fwd for the same block pair: the exact gradient of
+ * sum(dout * out) given the FINAL out and lse of the rows (for a ring, the
+ * merged ones), i.e. P = exp(s - lse), dS = P (dP - rowsum(dout*out)).
+ *   dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype` (overwritten; dk/dv are summed
+ *   over the Hq/Hkv query heads of each key/value head).
+ *   workspace: >= cp_workspace_size(CP_OP_BLOCK_BWD, ...) bytes (fp32 accumulators). */
+CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
+                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------- ring merge */
+
+/* Merge two partial attentions over disjoint key sets ("Ring Attention":
+ * lse = log(e^lse1 + e^lse2), o = o1 e^(lse1-lse) + o2 e^(lse2-lse)).
+ *   o1, o2, o [Sq,H,D] in `o_dtype` (CP_F32 or CP_BF16); lse1, lse2, lse [H,Sq] fp32.
+ *   o may alias o1 and lse may alias lse1 (in-place accumulation).
+ *   A row with both parts empty (-inf) stays empty (lse = -inf, o = 0). */
+CP_API cp_status cp_lse_merge(const void* o1, const float* lse1, const void* o2, const float* lse2,
+                       void* o, float* lse, int64_t Sq, int32_t H, int32_t D, int32_t o_dtype,
+                       void* stream);
+
+/* ---------------------------------------------------------------- Ulysses exchange */
+
+/* Sequence -> head exchange of P virtual ranks ("Ulysses": seq_to_head, one
+ * all-to-all, here an in-HBM permute).
+ *   x [S,H,D] (= rank r's slice [S/P,H,D] at rows r*S/P) -> y [P][S][H/P][D],
+ *   y[p][s][h'][:] = x[s][p*H/P + h'][:].  Requires S % P == 0, H % P == 0,
+ *   (H/P)*D*sizeof(dtype) % 16 == 0.  Bit-exact; x and y must not overlap. */
+CP_API cp_status cp_ulysses_seq2head(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                              int32_t dtype, void* stream);
+/* Inverse (head_to_seq): y [P][S][H/P][D] -> x [S,H,D]. */
+CP_API cp_status cp_ulysses_head2seq(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                              int32_t dtype, void* stream);
+
+/* ---------------------------------------------------------------- load-balancing reorders */
+
+/* Zigzag / DUAL_CHUNK_SWAP ("The zigzag partition"): y = the ranks' holdings
+ * concatenated in rank order: rank r's rows [r*2C, (r+1)*2C) are chunk r then
+ * chunk 2P-1-r of x, C = S/(2P).  Requires S % (2P) == 0.  Rows are H*D
+ * elements (H may be any head count).  Bit-exact; x and y must not overlap. */
+CP_API cp_status cp_zigzag_reorder(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                            int32_t dtype, void* stream);
+CP_API cp_status cp_zigzag_restore(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                            int32_t dtype, void* stream);
+
+/* Striped: y[r*(S/P) + i] = x[i*P + r] (rank r holds positions r, r+P, ...).
+ * Requires S % P == 0.  Bit-exact; x and y must not overlap. */
+CP_API cp_status cp_striped_reorder(const void* x, void* y, int64_t S, int32_t H, int32_t D, int32_t P,
+                             int32_t dtype, void* stream);
+CP_API cp_status cp_striped_restore(const void* y, void* x, int64_t S, int32_t H, int32_t D, int32_t P,
+                             int32_t dtype, void* stream);
+
+/* The same row maps applied to the columns of an lse [H,S] fp32 array:
+ * inverse = 0 takes sequence order to the ranks' order, inverse = 1 back.
+ * reorder is CP_REORDER_DUAL_CHUNK_SWAP or CP_REORDER_STRIPED. */
+CP_API cp_status cp_lse_reorder(const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                                int32_t reorder, int32_t inverse, void* stream);
+
+/* ---------------------------------------------------------------- drivers */
+
+/* Causal ring attention over P virtual ranks ("Ring Attention" with the
+ * layout of `reorder`).  q [S,Hq,D], k/v [S,Hkv,D], out [S,Hq,D] and lse [Hq,S]
+ * are in ORIGINAL sequence order; the driver reorders q/k/v into the
+ * workspace, runs the ring (skipping key blocks with no visible pair), and
+ * restores out.  cu_seqlens (device, n_docs+1) packs documents; packing is
+ * accepted only with a load-balanced layout (DUAL_CHUNK_SWAP, STRIPED or AUTO),
+ * as in the MaxText packing PR.  Requires S % P == 0 (S % 2P for
+ * DUAL_CHUNK_SWAP), 1 <= P <= 32.  workspace >= cp_workspace_size(CP_OP_RING_FWD). */
+CP_API cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                            int32_t mode, const int32_t* cu_seqlens, int32_t n_docs, void* out,
+                            float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* The ring of cp_ring_attention on buffers ALREADY in the ranks' layout (the
+ * output of cp_zigzag_reorder / cp_striped_reorder, or sequence order for
+ * CONTIGUOUS), as a data loader that shards by rank would deliver them:
+ * q/k/v/out rows and lse [Hq,S] columns are in rank order; cu_seqlens is in
+ * sequence positions.  No reorder or restore is done.  FUSED needs no
+ * workspace (may be NULL); STEPWISE needs cp_workspace_size(CP_OP_RING_FWD_REORDERED)
+ * bytes for its fp32 partial results. */
+CP_API cp_status cp_ring_attention_reordered(const void* q, const void* k, const void* v, int64_t S,
+                                             int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                                             int32_t P, int32_t reorder, int32_t mode,
+                                             const int32_t* cu_seqlens, int32_t n_docs, void* out,
+                                             float* lse, void* workspace, size_t ws_bytes,
+                                             void* stream);
+
+/* Backward of cp_ring_attention: dq [S,Hq,D], dk/dv [S,Hkv,D] (original
+ * order) from the forward's out and lse and the upstream gradient dout.
+ * Every (query block, key block) pair the ring visits is differentiated with
+ * the final merged lse; dK/dV of a key/value head are summed over its query
+ * heads.  workspace >= cp_workspace_size(CP_OP_RING_BWD). */
+CP_API cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, int64_t S, int32_t Hq,
+                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                                const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
+                                void* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/* Ulysses attention over P virtual ranks ("Ulysses"): seq2head of q, k, v;
+ * full-sequence causal attention of each rank's Hq/P query heads (Hkv/P
+ * key/value heads); head2seq of out.  Requires Hq % P == 0 and Hkv % P == 0
+ * (the degree cannot exceed the key/value head count), S % P == 0.
+ * out [S,Hq,D], lse [Hq,S].  workspace >= cp_workspace_size(CP_OP_ULYSSES_FWD). */
+CP_API cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                               int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                               const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes needed by `op` (a cp_op) for these sizes; `mode` is the
+ * cp_ring_mode for CP_OP_RING_FWD and ignored otherwise.  For CP_OP_BLOCK_BWD
+ * pass S = max(Sq, Sk) (P is ignored).  Returns CP_OK and
+ * writes *bytes, or an error for invalid sizes. */
+CP_API cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                            int32_t dtype, int32_t P, int32_t mode, size_t* bytes);
+
+/* ---------------------------------------------------------------- status */
+
+/* Synchronises `stream`, then reports (and clears) the library's device error
+ * word: CP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the
+ * last check, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK. */
+CP_API cp_status cp_check_device_status(void* stream);
+
+/* Test hook for the bounded-wait path: launches one block that waits on a
+ * barrier nothing arrives on, with a limit of `timeout_us` microseconds
+ * (1..1000000).  The wait gives up, records CP_ERR_DEVICE_TIMEOUT in the device
+ * error word and the kernel returns; nothing faults or hangs. */
+CP_API cp_status cp_debug_bounded_wait(int32_t timeout_us, void* stream);
+
+CP_API const char* cp_status_string(int32_t status);
+/* Thread-local message describing the last refused or failed call on this thread. */
+CP_API const char* cp_last_error(void);
+/* Library version, "major.minor.patch". */
+CP_API const char* cp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_ATTN_H */

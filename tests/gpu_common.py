@@ -1,0 +1,62 @@
+"""Shared helpers for the GPU parity tests (inputs come from synth, expected
+values only from the oracle)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import context_causal_attention_tcgen05_gb300 as cpa
+
+# Spec tolerances: max |err| of attention outputs (bf16 2e-2, fp32 1e-4), of lse 5e-3.
+TOL_OUT = {torch.bfloat16: 2e-2, torch.float32: 1e-4}
+TOL_LSE = 5e-3
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if not os.path.exists(cpa.library_path()):
+        from context_causal_attention_tcgen05_gb300 import build_lib
+        build_lib.build()
+    cpa.load_library()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def max_err(gpu, ref):
+    g = f64(gpu) if isinstance(gpu, torch.Tensor) else np.asarray(gpu, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    both_inf = np.isneginf(g) & np.isneginf(r)
+    d = np.abs(np.where(both_inf, 0.0, g - r))
+    return float(np.nan_to_num(d, nan=np.inf).max()) if d.size else 0.0
+
+
+def assert_close(gpu_out, gpu_lse, ref_out, ref_lse, dtype, what=""):
+    eo = max_err(gpu_out, ref_out)
+    el = max_err(gpu_lse, ref_lse)
+    assert eo <= TOL_OUT[dtype], f"{what}: out max err {eo}"
+    assert el <= TOL_LSE, f"{what}: lse max err {el}"
+    return eo, el
+
+
+def check_ok():
+    st = cpa.cp_check_device_status()
+    assert st == 0, f"device status {st}: {cpa.cp_last_error()}"
+
+
+def sample_rows(S, P, layout, n_random=256, seed=1):
+    """Chunk-boundary rows of the layout plus random rows (sorted, unique)."""
+    rows = set()
+    nchunks = 2 * P if layout in ("zigzag", "dual_chunk_swap") else P
+    C = S // nchunks
+    for c in range(nchunks):
+        for r in (c * C, c * C + 1, c * C + C // 2, (c + 1) * C - 2, (c + 1) * C - 1):
+            if 0 <= r < S:
+                rows.add(r)
+    rng = np.random.default_rng(seed)
+    rows.update(rng.integers(0, S, size=n_random).tolist())
+    return np.array(sorted(rows), dtype=np.int64)

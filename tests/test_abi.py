@@ -1,0 +1,108 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/cp_attn.h declares, and refuses bad arguments with the
+documented status before touching the device."""
+import ctypes
+
+import pytest
+
+import context_causal_attention_tcgen05_gb300 as cpa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import os
+    if not os.path.exists(cpa.library_path()):
+        from context_causal_attention_tcgen05_gb300 import build_lib
+        build_lib.build()
+    return cpa.load_library()
+
+
+def test_every_header_function_is_exported(lib):
+    names = cpa.header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert cpa.cp_status_string(0) == "CP_OK"
+    assert cpa.cp_status_string(-8) == "CP_ERR_DEVICE_TIMEOUT"
+    assert cpa.cp_version().count(".") == 2
+
+
+P16 = ctypes.c_void_p(1 << 20)  # 16-byte aligned fake device address; never dereferenced
+
+
+def _fwd(lib, **kw):
+    args = dict(q=P16, k=P16, v=P16, Sq=128, Sk=128, Hq=8, Hkv=8, D=128, dtype=1, mask=None,
+                scale=0.0, out=P16, lse=P16, stream=None)
+    args.update(kw)
+    return lib.cp_attn_block_fwd(*args.values())
+
+
+def test_block_fwd_refusals(lib):
+    assert _fwd(lib, dtype=7) == -3                       # CP_ERR_DTYPE
+    assert _fwd(lib, D=96) == -3                          # bf16 needs D in {64,128}
+    assert _fwd(lib, dtype=0, D=48) == -2                 # fp32 D not supported
+    assert _fwd(lib, Hq=6, Hkv=4) == -2                   # Hq % Hkv
+    assert _fwd(lib, Sq=-1) == -1
+    assert _fwd(lib, q=ctypes.c_void_p(0)) == -1          # NULL q
+    assert _fwd(lib, k=ctypes.c_void_p((1 << 20) + 8)) == -4  # misaligned
+    assert "aligned" in cpa.cp_last_error()
+    m = cpa.cp_mask()
+    m.causal, m.q_stride, m.k_stride = 1, 0, 1
+    assert _fwd(lib, mask=ctypes.byref(m)) == -1          # stride 0
+    assert _fwd(lib, Sq=0) == 0                           # empty is a no-op
+
+
+def _ring(lib, **kw):
+    args = dict(q=P16, k=P16, v=P16, S=8192, Hq=32, Hkv=32, D=128, dtype=1, P=8, reorder=1, mode=0,
+                cu=None, n_docs=0, out=P16, lse=P16, ws=P16, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return lib.cp_ring_attention(*args.values())
+
+
+def test_ring_refusals(lib):
+    assert _ring(lib, S=8200) == -2                       # S % 2P
+    assert _ring(lib, P=0) == -1
+    assert _ring(lib, P=33) == -1
+    assert _ring(lib, reorder=9) == -1
+    assert _ring(lib, mode=5) == -1
+    assert _ring(lib, P=20, S=20 * 64) == -5              # zigzag limited to P <= 16
+    # packing only with a load-balanced ring (MaxText packing PR)
+    assert _ring(lib, reorder=0, cu=P16, n_docs=3) == -5
+    assert "load-balanced" in cpa.cp_last_error()
+    assert _ring(lib, ws_bytes=100) == -6                 # workspace too small
+    assert _ring(lib, ws=ctypes.c_void_p(0)) == -6
+
+
+def test_ulysses_refusals(lib):
+    f = lib.cp_ulysses_attention
+    base = [P16, P16, P16, 32768, 32, 8, 128, 1, 16, None, 0, P16, P16, P16, 1 << 40, None]
+    a = list(base)
+    st = f(*a)  # Hkv=8 < P=16: degree limited by the key/value heads
+    assert st == -2 and "Hkv" in cpa.cp_last_error()
+    a = list(base)
+    a[5] = 32
+    a[3] = 32769
+    assert f(*a) == -2                                    # S % P
+
+
+def test_permute_refusals(lib):
+    assert lib.cp_ulysses_seq2head(P16, P16, 64, 6, 128, 4, 1, None) == -2   # H % P
+    assert lib.cp_zigzag_reorder(P16, P16, 60, 8, 128, 4, 1, None) == -2     # S % 2P
+    assert lib.cp_striped_reorder(P16, P16, 64, 1, 4, 4, 1, None) == -4      # 8-byte rows
+    assert lib.cp_zigzag_reorder(P16, P16, 64, 8, 128, 4, 1, None) == -1     # x, y overlap
+    assert lib.cp_zigzag_reorder(P16, P16, 0, 8, 128, 4, 1, None) == 0       # empty
+
+
+def test_merge_and_workspace_refusals(lib):
+    assert lib.cp_lse_merge(P16, P16, P16, P16, P16, P16, 16, 4, 100, 1, None) == -4
+    assert lib.cp_lse_merge(P16, P16, P16, P16, P16, P16, 16, 4, 128, 5, None) == -3
+    out = ctypes.c_size_t(0)
+    assert lib.cp_workspace_size(9, 8192, 32, 32, 128, 1, 8, 0, ctypes.byref(out)) == -1
+    assert lib.cp_workspace_size(0, 8192, 32, 32, 128, 1, 8, 0, ctypes.byref(out)) == 0
+    fused = out.value
+    assert lib.cp_workspace_size(0, 8192, 32, 32, 128, 1, 8, 1, ctypes.byref(out)) == 0
+    assert out.value > fused  # stepwise keeps fp32 partials
+    assert lib.cp_debug_bounded_wait(0, None) == -1

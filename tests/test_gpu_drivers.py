@@ -1,0 +1,148 @@
+"""GPU parity of the ring and Ulysses drivers (P virtual ranks on one GPU)
+against UNPARTITIONED attention computed by the CPU oracle.
+
+Small sizes are compared element by element; the full-size workloads (the
+sizes and launch configuration the bench times) are compared on sampled rows
+(every head; chunk-boundary rows plus random rows), which the oracle can
+compute one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import context_causal_attention_tcgen05_gb300 as cpa
+import oracle
+from gpu_common import TOL_OUT, assert_close, check_ok, f64, max_err, need_gpu, sample_rows
+from synth import cu_seqlens_from_lengths, doc_lengths, make_inputs, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+LAYOUTS = ["contiguous", "zigzag", "striped"]
+MODES = ["fused", "stepwise"]
+
+
+# ---------------------------------------------------------------- the handbook's tiny workload (fp32)
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_exact_ring(layout, mode):
+    q, k, v = make_qkv()  # S=32, H=8, D=16, seed 0
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), 4, layout, mode)
+    assert_close(o, l, ref_o, ref_l, torch.float32, f"ring {layout} {mode}")
+    check_ok()
+
+
+def test_tiny_exact_ulysses():
+    q, k, v = make_qkv()
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), 4)
+    assert_close(o, l, ref_o, ref_l, torch.float32, "ulysses")
+    check_ok()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tiny_exact_ring_bwd(layout):
+    q, k, v = make_qkv()
+    g = torch.Generator().manual_seed(5)
+    do = torch.randn(q.shape, generator=g)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), 4, layout)
+    dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), 4, layout)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert max_err(got, ref) <= 1e-4 * max(1.0, float(np.abs(ref).max())), name
+    check_ok()
+
+
+# ---------------------------------------------------------------- medium bf16, element by element
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("mode", MODES)
+def test_ring_bf16_medium(layout, mode):
+    S, Hq, Hkv, D, P = 1024, 8, 2, 128, 4
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=3)
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, mode)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"{layout} {mode}")
+    check_ok()
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_ring_bf16_packed_medium(layout):
+    S, Hq, Hkv, D, P = 2048, 4, 2, 128, 4
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=4)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 700, seed=2))
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, "fused",
+                                 cu_seqlens=torch.from_numpy(cu).cuda())
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, layout)
+    check_ok()
+
+
+@pytest.mark.parametrize("Hq,Hkv,P", [(8, 8, 4), (8, 4, 4), (16, 8, 8)])
+def test_ulysses_bf16_medium(Hq, Hkv, P):
+    S, D = 1024, 128
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=6)
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), P)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, "ulysses")
+    check_ok()
+
+
+def test_ring_bwd_bf16_medium():
+    S, Hq, Hkv, D, P = 512, 4, 1, 128, 4
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=7, with_dout=True)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag")
+    dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, "zigzag")
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+    check_ok()
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled rows
+
+def _sampled_check(q, k, v, o, l, rows, cu=None, what=""):
+    S = k.shape[0]
+    ref_o, ref_l = oracle.attention(q[rows], k, v, True, pos_q=rows, pos_k=np.arange(S), cu_seqlens=cu)
+    o_s = o[torch.from_numpy(rows).cuda()]
+    l_s = l[:, torch.from_numpy(rows).cuda()]
+    return assert_close(o_s, l_s, ref_o, ref_l, torch.bfloat16, what)
+
+
+def test_full_ring_fwd_mha_s8192_p8_zigzag():
+    S, H, D, P = 8192, 32, 128, 8
+    q, k, v = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag", "fused")
+    check_ok()
+    _sampled_check(q, k, v, o, l, sample_rows(S, P, "zigzag", 192), what="ring s8192")
+    o2, l2 = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag", "stepwise")
+    check_ok()
+    _sampled_check(q, k, v, o2, l2, sample_rows(S, P, "zigzag", 64, seed=2), what="ring s8192 stepwise")
+
+
+def test_full_ulysses_s32768_h32_p16():
+    S, H, D, P = 32768, 32, 128, 16
+    q, k, v = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), P)
+    check_ok()
+    _sampled_check(q, k, v, o, l, sample_rows(S, P, "contiguous", 48), what="ulysses s32768")
+
+
+def test_full_packed_varlen_s131072_p8():
+    S, Hq, Hkv, D, P = 131072, 32, 8, 128, 8
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=0)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 512, 16384, seed=0))
+    cu_d = torch.from_numpy(cu).cuda()
+    rows = sample_rows(S, P, "striped", 24)
+    rows = np.unique(np.concatenate([rows, cu[1:-1], cu[1:-1] - 1]))  # document boundaries
+    for layout in ("striped", "zigzag"):
+        o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, "fused", cu_seqlens=cu_d)
+        check_ok()
+        _sampled_check(q, k, v, o, l, rows, cu=cu, what=f"packed {layout}")

@@ -1,0 +1,188 @@
+"""GPU parity of the individual kernels against the CPU oracle, through the C ABI.
+
+Permutes and reorders must be bit-exact; attention and merge results must
+meet the tolerances fixed for this method (out: 2e-2 bf16 / 1e-4 fp32 max
+abs; lse: 5e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import context_causal_attention_tcgen05_gb300 as cpa
+import oracle
+from gpu_common import TOL_LSE, TOL_OUT, assert_close, check_ok, f64, max_err, need_gpu
+from synth import cu_seqlens_from_lengths, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _raw(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def _rand(shape, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(dtype)
+
+
+# ---------------------------------------------------------------- reorders and permutes (bit-exact)
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("S,H,D,P", [(64, 4, 8, 4), (96, 2, 16, 3), (8192, 32, 128, 8), (131072, 8, 128, 8)])
+def test_zigzag_and_striped_bitexact(dtype, S, H, D, P):
+    x = _rand((S, H, D), dtype, 11)
+    xd = x.cuda()
+    raw = _raw(x).numpy()
+    for name, layout in (("zigzag", "zigzag"), ("striped", "striped")):
+        if layout == "zigzag" and S % (2 * P):
+            continue
+        y = getattr(cpa, f"cp_{name}_reorder")(xd, P)
+        want = oracle.reorder(raw, P, layout)
+        assert np.array_equal(_raw(y.cpu()).numpy(), want), name
+        back = getattr(cpa, f"cp_{name}_restore")(y, P)
+        assert torch.equal(_raw(back.cpu()), _raw(x)), name + " restore"
+    check_ok()
+
+
+@pytest.mark.parametrize("dtype,S,H,D,P", [
+    (torch.float32, 32, 8, 16, 4),         # the handbook's tiny workload
+    (torch.bfloat16, 32768, 32, 128, 16),  # llama2-7b attention shape, 2 heads per rank
+    (torch.bfloat16, 4096, 8, 128, 8),     # one head per rank (GQA key/value side)
+    (torch.float32, 48, 6, 8, 3),
+])
+def test_ulysses_permute_bitexact(dtype, S, H, D, P):
+    x = _rand((S, H, D), dtype, 12)
+    xd = x.cuda()
+    y = cpa.cp_ulysses_seq2head(xd, P)
+    want = oracle.ulysses_seq2head(_raw(x).numpy(), P)
+    assert np.array_equal(_raw(y.cpu()).numpy(), want)
+    back = cpa.cp_ulysses_head2seq(y, P)
+    assert torch.equal(_raw(back.cpu()), _raw(x))
+    check_ok()
+
+
+# ---------------------------------------------------------------- LSE merge
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("Sq,H,D", [(1, 1, 64), (333, 8, 128), (4096, 32, 128)])
+def test_lse_merge(dtype, Sq, H, D):
+    g = torch.Generator().manual_seed(21)
+    o1 = torch.randn(Sq, H, D, generator=g).to(dtype)
+    o2 = torch.randn(Sq, H, D, generator=g).to(dtype)
+    l1 = torch.randn(H, Sq, generator=g) * 4
+    l2 = torch.randn(H, Sq, generator=g) * 4
+    # empty parts: some rows only in one part, some in neither
+    l1[:, ::7] = -float("inf")
+    l2[:, ::5] = -float("inf")
+    o1[::7] = 0
+    o2[::5] = 0
+    ref_o, ref_l = oracle.lse_merge(f64(o1), f64(l1), f64(o2), f64(l2))
+    o, l = cpa.cp_lse_merge(o1.cuda(), l1.cuda(), o2.cuda(), l2.cuda())
+    tol = 1e-5 if dtype == torch.float32 else 2e-2
+    assert max_err(o, ref_o) <= tol
+    assert max_err(l, ref_l) <= 1e-5
+    # in place into (o1, lse1)
+    a, b = o1.cuda(), l1.cuda()
+    cpa.cp_lse_merge(a, b, o2.cuda(), l2.cuda(), out=a, lse=b)
+    assert max_err(a, ref_o) <= tol and max_err(b, ref_l) <= 1e-5
+    check_ok()
+
+
+# ---------------------------------------------------------------- block attention forward
+
+FWD_CASES = [
+    # Sq, Sk, Hq, Hkv, D, q_off, k_off, q_stride, k_stride, docs
+    (33, 33, 4, 4, 16, 0, 0, 1, 1, None),
+    (17, 40, 4, 2, 32, 40, 0, 1, 1, None),            # later queries against an earlier block
+    (1, 129, 2, 1, 64, 200, 0, 1, 1, None),           # single row
+    (129, 129, 4, 1, 128, 0, 0, 1, 1, None),          # ragged tail past one 128-row tile
+    (300, 260, 4, 2, 128, 100, 60, 1, 1, None),       # offsets, several tiles, ragged
+    (64, 64, 2, 2, 64, 3, 1, 4, 4, None),             # striped rank 3 vs rank 1 (P=4)
+    (64, 64, 2, 2, 64, 1, 3, 4, 4, None),             # striped rank 1 vs rank 3 (first row empty)
+    (256, 256, 4, 2, 128, 0, 0, 1, 1, [50, 1, 77, 128]),   # packed documents
+    (20, 30, 2, 2, 64, 0, 25, 1, 1, None),            # every row fully masked
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("case", FWD_CASES)
+def test_block_fwd(dtype, case):
+    Sq, Sk, Hq, Hkv, D, qo, ko, qs, ks, docs = case
+    if dtype == torch.bfloat16 and D not in (64, 128):
+        pytest.skip("bf16 path is D in {64, 128}")
+    g = torch.Generator().manual_seed(31)
+    q = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    k = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    ref_o, ref_l = oracle.attention(q, k, v, True, qo, ko, q_stride=qs, k_stride=ks, cu_seqlens=cu)
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, qs, ks, cu_d)
+    assert_close(o, l, ref_o, ref_l, dtype, str(case))
+    check_ok()
+
+
+# ---------------------------------------------------------------- block attention backward
+
+BWD_CASES = [
+    (33, 33, 4, 4, 16, 0, 0, None),
+    (40, 50, 4, 2, 64, 60, 20, None),
+    (130, 130, 4, 1, 128, 0, 0, None),
+    (96, 96, 2, 2, 64, 0, 0, [10, 50, 36]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("case", BWD_CASES)
+def test_block_bwd(dtype, case):
+    Sq, Sk, Hq, Hkv, D, qo, ko, docs = case
+    if dtype == torch.bfloat16 and D not in (64, 128):
+        pytest.skip("bf16 path is D in {64, 128}")
+    g = torch.Generator().manual_seed(41)
+    q = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    k = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    do = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    # forward on the GPU gives the (out, lse) the backward consumes, as in training
+    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, 1, 1, cu_d)
+    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, True, qo, ko, 1, 1, cu_d)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, qo, ko, cu_seqlens=cu)
+    tol = TOL_OUT[dtype] if dtype == torch.float32 else 2e-2
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = max_err(got, ref)
+        scale = max(1.0, float(np.abs(ref).max()))
+        assert e <= tol * scale, f"{name} {case}: {e}"
+    check_ok()
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_bounded_wait_gives_up_and_reports():
+    assert cpa.cp_check_device_status() == 0
+    cpa.cp_debug_bounded_wait(20000)  # 20 ms on a barrier nothing arrives on
+    st = cpa.cp_check_device_status()
+    assert st == -8, st
+    assert "bounded wait" in cpa.cp_last_error()
+    assert cpa.cp_check_device_status() == 0  # cleared
+    # the context is still usable
+    x = torch.ones(16, device="cuda")
+    assert float(x.sum()) == 16.0
+
+
+@pytest.mark.parametrize("S,H,P", [(64, 3, 4), (8192, 32, 8)])
+def test_lse_reorder_bitexact(S, H, P):
+    x = torch.randn(H, S, generator=torch.Generator().manual_seed(13))
+    for layout in ("zigzag", "striped"):
+        y = cpa.cp_lse_reorder(x.cuda(), P, layout)
+        want = oracle.reorder(x.numpy().T, P, layout).T
+        assert np.array_equal(y.cpu().numpy(), want)
+        back = cpa.cp_lse_reorder(y, P, layout, inverse=True)
+        assert torch.equal(back.cpu(), x)
+    check_ok()
