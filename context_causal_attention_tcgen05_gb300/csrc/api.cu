@@ -237,9 +237,8 @@ int32_t resolve_layout(int32_t reorder, const int32_t* cu) {
 
 cp_status launch_fwd(const AttnArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
                      int64_t k_rows, cudaStream_t st) {
-  (void)q_rows;
-  (void)k_rows;
-  return launch_attn_fwd_simt(a, s, dtype == CP_BF16, st);
+  if (dtype == CP_BF16) return launch_attn_fwd_tc(a, s, q_rows, k_rows, st);
+  return launch_attn_fwd_simt(a, s, 0, st);
 }
 
 cp_status launch_bwd(const BwdArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,

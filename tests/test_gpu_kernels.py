@@ -32,7 +32,7 @@ def _rand(shape, dtype, seed):
 
 # ---------------------------------------------------------------- reorders and permutes (bit-exact)
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("S,H,D,P", [(64, 4, 8, 4), (96, 2, 16, 3), (8192, 32, 128, 8), (131072, 8, 128, 8)])
 def test_zigzag_and_striped_bitexact(dtype, S, H, D, P):
     x = _rand((S, H, D), dtype, 11)
@@ -68,7 +68,7 @@ def test_ulysses_permute_bitexact(dtype, S, H, D, P):
 
 # ---------------------------------------------------------------- LSE merge
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("Sq,H,D", [(1, 1, 64), (333, 8, 128), (4096, 32, 128)])
 def test_lse_merge(dtype, Sq, H, D):
     g = torch.Generator().manual_seed(21)
@@ -109,7 +109,7 @@ FWD_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("case", FWD_CASES)
 def test_block_fwd(dtype, case):
     Sq, Sk, Hq, Hkv, D, qo, ko, qs, ks, docs = case
@@ -137,7 +137,7 @@ BWD_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("case", BWD_CASES)
 def test_block_bwd(dtype, case):
     Sq, Sk, Hq, Hkv, D, qo, ko, docs = case
