@@ -243,8 +243,8 @@ cp_status launch_fwd(const AttnArgs& a, Schedule& s, int32_t dtype, int64_t q_ro
 
 cp_status launch_bwd(const BwdArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
                      int64_t k_rows, cudaStream_t st) {
-  (void)q_rows;
-  (void)k_rows;
+  // The tensor-core backward is written for D = 128; other head sizes use the FFMA kernel.
+  if (dtype == CP_BF16 && a.D == 128) return launch_attn_bwd_tc(a, s, q_rows, k_rows, st);
   return launch_attn_bwd_simt(a, s, dtype == CP_BF16, st);
 }
 

@@ -146,3 +146,43 @@ def test_full_packed_varlen_s131072_p8():
         o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, "fused", cu_seqlens=cu_d)
         check_ok()
         _sampled_check(q, k, v, o, l, rows, cu=cu, what=f"packed {layout}")
+
+
+def test_full_gqa_ring_fwd_bwd_s65536_p4_zigzag():
+    """The llama3.1-8b attention shape (Hq=32, Hkv=8), fwd + bwd through the ring.
+
+    Checked exactly where the oracle can compute outputs one by one: forward
+    rows (sampled), dQ rows (sampled; a row's gradient needs only that row),
+    dK/dV of the LAST 64 key rows (only the last 64 queries see them), plus
+    two identities that hold at any size: sum_j dV_j = sum of dO over the
+    group's query heads (rows of P sum to 1) and sum_j dK_j = 0 (each row of
+    dS sums to 0)."""
+    S, Hq, Hkv, D, P = 65536, 32, 8, 128, 4
+    G = Hq // Hkv
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=0, with_dout=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, l = cpa.cp_ring_attention(qd, kd, vd, P, "zigzag", "fused")
+    check_ok()
+    rows = sample_rows(S, P, "zigzag", 24)
+    _sampled_check(q, k, v, o, l, rows, what="gqa fwd")
+    dq, dk, dv = cpa.cp_ring_attention_bwd(qd, kd, vd, o, l, dod, P, "zigzag")
+    check_ok()
+    allpos = np.arange(S)
+    # dQ on sampled rows
+    rq, _, _ = oracle.attention_bwd(q[rows], k, v, do[rows], True, pos_q=rows, pos_k=allpos)
+    e = max_err(dq[torch.from_numpy(rows).cuda()], rq)
+    assert e <= 2e-2 * max(1.0, float(np.abs(rq).max())), f"dq {e}"
+    # dK / dV of the last T key rows
+    T = 64
+    tail = np.arange(S - T, S)
+    _, rk, rv = oracle.attention_bwd(q[S - T:], k, v, do[S - T:], True, pos_q=tail, pos_k=allpos)
+    for name, got, ref in (("dk", dk[S - T:], rk[S - T:]), ("dv", dv[S - T:], rv[S - T:])):
+        e = max_err(got, ref)
+        assert e <= 2e-2 * max(1.0, float(np.abs(ref).max())), f"{name} {e}"
+    # identities over all rows (fp64 sums of the GPU result vs of the inputs)
+    dv_sum = dv.double().sum(0).cpu().numpy()             # [Hkv, D]
+    do_sum = do.double().sum(0).reshape(Hkv, G, D).sum(1).numpy()
+    assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(1.0, np.abs(do_sum).max()), "sum dV"
+    dk_sum = dk.double().sum(0).cpu().numpy()
+    dk_scale = dk.double().abs().sum(0).cpu().numpy().max()
+    assert np.abs(dk_sum).max() <= 1e-3 * dk_scale, "sum dK"
