@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcp_attn.
 
 __all__ = [
     "CpAttnError", "load_library", "library_path", "header_functions",
-    "cp_attn_block_fwd", "cp_attn_block_bwd", "cp_lse_merge",
+    "cp_attn_block_fwd", "cp_attn_block_bwd", "cp_attn_block_bwd_noalloc", "cp_lse_merge",
     "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
     "cp_lse_reorder",
@@ -50,6 +50,8 @@ _SIGS = {
                           ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p],
     "cp_attn_block_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32,
                           _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
+    "cp_attn_block_bwd_noalloc": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32,
+                                  _c_i32, _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_p],
     "cp_lse_merge": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p],
     "cp_ulysses_seq2head": [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
     "cp_ulysses_head2seq": [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
@@ -203,6 +205,24 @@ def cp_attn_block_bwd(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
         ctypes.byref(m), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return dq, dk, dv
+
+
+def cp_attn_block_bwd_noalloc(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0,
+                              q_stride=1, k_stride=1, cu_seqlens=None, scale=0.0, dq=None, dk=None,
+                              dv=None, stream=None):
+    """cp_attn_block_bwd without a workspace: the library uses its built-in
+    32 MiB scratch array and allocates nothing (outputs are allocated here
+    unless passed in)."""
+    Sq, Hq, D = q.shape
+    Sk, Hkv, _ = k.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens)
+    _check("cp_attn_block_bwd_noalloc", load_library().cp_attn_block_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
+        ctypes.byref(m), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
 
 

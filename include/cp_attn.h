@@ -132,6 +132,30 @@ CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, 
                             void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                             void* stream);
 
+/* cp_attn_block_bwd without a workspace and without any allocation (the pages
+ * have no counterpart: this is a library facility).  For callers that may not
+ * allocate device memory and have no workspace to hand over: code running
+ * behind a plugin or custom-operator interface that passes only input and
+ * output buffers, runtimes that plan all device memory ahead of time and
+ * forbid allocation afterwards, or processes whose allocator belongs to
+ * another runtime.  Arguments, layouts and results are those of
+ * cp_attn_block_bwd minus the workspace.
+ *   Scratch: a 32 MiB array built into the library (every GPU that loads the
+ *   library keeps it until the process exits).  Sizes whose scratch
+ *   (4*Hq*Sq + 4*D*(Hq*Sq + 2*Hkv*Sk) bytes, each part rounded up to 256) does
+ *   not fit return CP_ERR_UNSUPPORTED with a message; nothing is launched.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (each call
+ *   clears what must start at zero): calls that overlap on the GPU race, so
+ *   serialise them (one stream per device). */
+CP_API cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, const void* v,
+                                           const void* out, const void* dout, const float* lse,
+                                           int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv,
+                                           int32_t D, int32_t dtype, const cp_mask* mask,
+                                           float scale, void* dq, void* dk, void* dv,
+                                           void* stream);
+
 /* ---------------------------------------------------------------- ring merge */
 
 /* Merge two partial attentions over disjoint key sets ("Ring Attention":
