@@ -226,6 +226,49 @@ def bench_ours(args):
 
     launches_per_step = 6
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def gqa_fwd_bwd(n_steps):
+        """fwd and fwd+bwd of the GQA ring workload (S=65536, Hq=32, Hkv=8, D=128,
+        P=4, zigzag) through the public drivers, device-resident inputs."""
+        S4, Hq4, Hkv4, D4, P4 = 65536, 32, 8, 128, 4
+        q4, k4, v4, do4 = (t.to(dev) for t in make_inputs(S4, Hq4, Hkv4, D4, torch.bfloat16, 0, True))
+        o4, l4 = torch.empty_like(q4), torch.empty(Hq4, S4, dtype=torch.float32, device=dev)
+        dq4, dk4, dv4 = torch.empty_like(q4), torch.empty_like(k4), torch.empty_like(v4)
+        wf = torch.empty(cpa.cp_workspace_size("ring_fwd", S4, Hq4, Hkv4, D4, torch.bfloat16, P4),
+                         dtype=torch.uint8, device=dev)
+        wb = torch.empty(cpa.cp_workspace_size("ring_bwd", S4, Hq4, Hkv4, D4, torch.bfloat16, P4),
+                         dtype=torch.uint8, device=dev)
+
+        def one(ev=None):
+            if ev:
+                ev[0].record(stream)
+            cpa.cp_ring_attention(q4, k4, v4, P4, "zigzag", "fused", out=o4, lse=l4, workspace=wf)
+            if ev:
+                ev[1].record(stream)
+            cpa.cp_ring_attention_bwd(q4, k4, v4, o4, l4, do4, P4, "zigzag", dq=dq4, dk=dk4, dv=dv4,
+                                      workspace=wb)
+            if ev:
+                ev[2].record(stream)
+
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(n_steps):
+            flush.fill_(1.0)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            one(ev)
+            evs.append(ev)
+        torch.cuda.synchronize()
+        fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        f = causal_flop(S4, Hq4, D4)
+        del q4, k4, v4, do4, o4, l4, dq4, dk4, dv4, wf, wb
+        return {"workload": "gqa_ring_fwd_bwd_s65536_hq32_hkv8_d128_bf16_p4_zigzag",
+                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": f / (fwd_ms * 1e-3) / 1e12,
+                "bwd_tflops": 2.5 * f / (bwd_ms * 1e-3) / 1e12,
+                "fwd_bwd_tflops": 3.5 * f / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                "flop_fwd": f, "flop_bwd": 2.5 * f, "steps": n_steps}
     for _ in range(args.warmup):
         step(mk())
     torch.cuda.synchronize()
@@ -248,6 +291,7 @@ def bench_ours(args):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
+    fb = gqa_fwd_bwd(args.fwd_bwd_steps) if args.fwd_bwd_steps > 0 else None
     sampler.mark_end()
     clocks = sampler.finish()
     st = cpa.cp_check_device_status()
@@ -323,6 +367,7 @@ def bench_ours(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "attn_fwd_tc (ring, fused)", "peak_source": peaks["source"] + " burst bf16"},
+            "fwd_bwd": None if fb is None else dict(fb, frac_of_peak=fb["fwd_bwd_tflops"] / peak),
             "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,
                       "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
                       "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},
@@ -342,8 +387,9 @@ def bench_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--fwd-bwd-steps", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
