@@ -134,27 +134,31 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def cpu_oracle_sample(q, k, v, target_s: float = 12.0):
-    """Times the float64 oracle on sampled query rows (all heads) of the workload.
-    Returns (TFLOP/s, rows, seconds)."""
+def _oracle_inputs(q, k, v):
+    return (q.float().numpy().astype(np.float64), k.float().numpy().astype(np.float64),
+            v.float().numpy().astype(np.float64))
+
+
+def _oracle_rows(qs, ks, vs, n, rng):
+    """Times the float64 oracle on n random query rows (all heads) against the full
+    causal key range; returns (FLOP of those rows, seconds)."""
     import oracle
 
+    rows = np.sort(rng.integers(0, S, size=n))
+    t0 = time.perf_counter()
+    oracle.attention(qs[rows], ks, vs, True, pos_q=rows, pos_k=np.arange(S))
+    dt = time.perf_counter() - t0
+    return 4.0 * D * H * float(np.sum(rows + 1)), dt
+
+
+def cpu_oracle_sample(q, k, v, target_s: float = 12.0):
+    """Oracle throughput on a bounded sample sized to about target_s seconds.
+    Returns (TFLOP/s, rows, seconds)."""
+    qs, ks, vs = _oracle_inputs(q, k, v)
     rng = np.random.default_rng(123)
-    qs = q.float().numpy().astype(np.float64)
-    ks = k.float().numpy().astype(np.float64)
-    vs = v.float().numpy().astype(np.float64)
-
-    def run(n):
-        rows = np.sort(rng.integers(0, S, size=n))
-        t0 = time.perf_counter()
-        oracle.attention(qs[rows], ks, vs, True, pos_q=rows, pos_k=np.arange(S))
-        dt = time.perf_counter() - t0
-        flop = 4.0 * D * H * float(np.sum(rows + 1))
-        return flop, dt, n
-
-    flop, dt, n = run(8)
-    n2 = int(max(8, min(4096, 8 * target_s / max(dt, 1e-3))))
-    flop, dt, n = run(n2)
+    _, dt = _oracle_rows(qs, ks, vs, 8, rng)
+    n = int(max(8, min(4096, 8 * target_s / max(dt, 1e-3))))
+    flop, dt = _oracle_rows(qs, ks, vs, n, rng)
     return flop / dt / 1e12, n, dt
 
 
@@ -165,13 +169,17 @@ def bench_reference(args):
     from synth import make_inputs
 
     q, k, v = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
+    qs, ks, vs = _oracle_inputs(q, k, v)
+    rng = np.random.default_rng(123)
+    # one calibration, then every step is the same bounded sample size (~90 s in all)
+    _, dt8 = _oracle_rows(qs, ks, vs, 8, rng)
+    per_step_s = min(1.0, 90.0 / max(1, args.steps + args.warmup))
+    n = int(max(1, min(4096, 8 * per_step_s / max(dt8, 1e-3))))
     per_step = []
-    rows_used = 0
     for i in range(args.warmup + args.steps):
-        tf, n, dt = cpu_oracle_sample(q, k, v, target_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
+        flop, dt = _oracle_rows(qs, ks, vs, n, rng)
         if i >= args.warmup:
-            per_step.append((tf, dt))
-            rows_used = n
+            per_step.append((flop / dt / 1e12, dt))
     value = statistics.mean(t for t, _ in per_step)
     ms = 1e3 * statistics.mean(d for _, d in per_step)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -181,7 +189,7 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seed 0",
         "config": {"workload": WORKLOAD, "S": S, "H": H, "D": D, "P": P, "reorder": "dual_chunk_swap"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows_used} random query rows x {H} heads per step, full causal key range"},
+                         "sample": f"{n} random query rows x {H} heads per step, full causal key range"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
