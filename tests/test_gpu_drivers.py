@@ -95,12 +95,17 @@ def test_ulysses_bf16_medium(Hq, Hkv, P):
     check_ok()
 
 
-def test_ring_bwd_bf16_medium():
-    S, Hq, Hkv, D, P = 512, 4, 1, 128, 4
+@pytest.mark.parametrize("layout,docs", [("zigzag", False), ("contiguous", False), ("striped", False),
+                                         ("zigzag", True), ("striped", True)])
+def test_ring_bwd_bf16_medium(layout, docs):
+    S, Hq, Hkv, D, P = 1024, 4, 1, 128, 4
     q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=7, with_dout=True)
-    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag")
-    dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, "zigzag")
-    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 500, seed=3)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, cu_seqlens=cu_d)
+    dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, layout,
+                                           cu_seqlens=cu_d)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
     check_ok()

@@ -130,17 +130,22 @@ def test_block_fwd(dtype, case):
 # ---------------------------------------------------------------- block attention backward
 
 BWD_CASES = [
-    (33, 33, 4, 4, 16, 0, 0, None),
-    (40, 50, 4, 2, 64, 60, 20, None),
-    (130, 130, 4, 1, 128, 0, 0, None),
-    (96, 96, 2, 2, 64, 0, 0, [10, 50, 36]),
+    # Sq, Sk, Hq, Hkv, D, q_off, k_off, docs, causal
+    (33, 33, 4, 4, 16, 0, 0, None, True),
+    (40, 50, 4, 2, 64, 60, 20, None, True),
+    (130, 130, 4, 1, 128, 0, 0, None, True),
+    (96, 96, 2, 2, 64, 0, 0, [10, 50, 36], True),
+    (300, 270, 4, 2, 128, 100, 50, None, True),        # several ragged tiles, offsets
+    (256, 256, 4, 2, 128, 0, 0, [70, 1, 100, 85], True),  # packed documents
+    (200, 150, 2, 1, 128, 0, 0, None, False),          # no mask at all
+    (192, 192, 2, 2, 128, 0, 0, [64, 128], False),     # documents without causality
 ]
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("case", BWD_CASES)
 def test_block_bwd(dtype, case):
-    Sq, Sk, Hq, Hkv, D, qo, ko, docs = case
+    Sq, Sk, Hq, Hkv, D, qo, ko, docs, causal = case
     if dtype == torch.bfloat16 and D not in (64, 128):
         pytest.skip("bf16 path is D in {64, 128}")
     g = torch.Generator().manual_seed(41)
@@ -151,9 +156,9 @@ def test_block_bwd(dtype, case):
     cu = None if docs is None else cu_seqlens_from_lengths(docs)
     cu_d = None if cu is None else torch.from_numpy(cu).cuda()
     # forward on the GPU gives the (out, lse) the backward consumes, as in training
-    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, 1, 1, cu_d)
-    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, True, qo, ko, 1, 1, cu_d)
-    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, qo, ko, cu_seqlens=cu)
+    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), causal, qo, ko, 1, 1, cu_d)
+    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, causal, qo, ko, 1, 1, cu_d)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal, qo, ko, cu_seqlens=cu)
     tol = TOL_OUT[dtype] if dtype == torch.float32 else 2e-2
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         e = max_err(got, ref)
