@@ -9,25 +9,27 @@
 // log-sum-exp merge (section "Ring Attention: passing the KV once around a
 // ring": lse = log(e^lse1 + e^lse2), o = o1 e^(lse1-lse) + o2 e^(lse2-lse)).
 //
-// One CTA = one 128-row query tile of one head; 6 warps:
-//   warp 0      TMA producer: Q once, then K and V tiles (128 keys) into a
-//               2-stage ring of 128B-swizzled shared-memory buffers.
-//   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM
-//               buffers (M=128, N=128, K=D), then O += P V into TMEM
-//               (M=128, N=D, K=128) once the softmax has written P.
-//               Issue order QK(j), PV(j-1) lets QK(j) overlap softmax(j-1).
-//   warps 2..5  softmax: thread t owns query row t (its TMEM lane): reads its
-//               S row with tcgen05.ld, applies the causal / document mask on
-//               boundary tiles only, keeps the running max in the log2
-//               domain, writes P (bf16) to shared memory in the MMA's K-major
-//               128B-swizzled layout, and rescales its O row in TMEM only when
-//               the max grew by more than 2^8 (otherwise the stale max is kept
-//               and the final normalisation absorbs it).
-// Key/value tiles entirely masked (after every query of the tile, or outside
-// the tile's documents) are never loaded; fully visible tiles skip the mask.
-// Every mbarrier wait is bounded; on expiry the CTA records
-// CP_ERR_DEVICE_TIMEOUT in the device error word, drains its own copies and
-// MMAs, frees its TMEM and returns.
+// One CTA = two 128-row query tiles (Q0, Q1) of one head, 12 warps:
+//   warps 0..3  softmax of Q0, warps 4..7 softmax of Q1: thread t owns query
+//               row t of its tile (its TMEM lane).  It reads its S row with
+//               tcgen05.ld, masks boundary tiles only, keeps the running max
+//               in the log2 domain, and writes P (bf16) back into the first 64
+//               columns of its S buffer with tcgen05.st.  O is rescaled in
+//               TMEM only when the max grew by more than 2^8 (otherwise the
+//               stale max is kept; the final normalisation absorbs it).
+//   warp 8      TMA producer: Q0/Q1 once, K and V tiles (128 keys) in 2-stage
+//               rings of 128B-swizzled shared-memory buffers.  (Warps 8..11 form
+//               the third warpgroup, which gives registers to the softmax ones.)
+//   warp 9      MMA issuer (one thread), ping-pong order per key tile j:
+//                 S0 = Q0 K_j^T | O1 += P1 V_{j-1} | S1 = Q1 K_j^T | O0 += P0 V_j
+//               so each softmax overlaps the other tile's two products.
+//               P is the A operand straight from TMEM (M=128 lanes, two bf16 per
+//               column); V is the B operand from shared memory (MN-major).
+// TMEM: S0/P0 cols 0..127, O0 128..255, S1/P1 256..383, O1 384..511.
+// Key/value tiles entirely masked for both query tiles are never loaded;
+// fully visible tiles skip the mask.  Every mbarrier wait is bounded; on
+// expiry the CTA records CP_ERR_DEVICE_TIMEOUT in the device error word,
+// drains its own copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -36,9 +38,16 @@
 namespace cpa {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kThreads = 192;
+constexpr int BM = 128;          // rows per query tile
+constexpr int kRowsPerCta = 2 * BM;
+constexpr int BN = 128;          // keys per key/value tile
+constexpr int kThreads = 384;        // 3 warpgroups
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;         // warps 10, 11 only rebalance registers
+// Register split (launch: 384 x 168 = 64512): the producer/MMA warpgroup drops to
+// 56, the two softmax warpgroups rise to 224: 128*56 + 256*224 = 64512.
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s when draining after an abort
@@ -48,12 +57,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D>
 struct Layout {
   static constexpr int kTile = 128 * D * 2;  // one 128-row tile of bf16 [rows][D]
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;      // 2 stages
+  static constexpr int kQ = 0;               // Q0, Q1
+  static constexpr int kK = kQ + 2 * kTile;  // 2 stages
   static constexpr int kV = kK + 2 * kTile;  // 2 stages
-  static constexpr int kP = kV + 2 * kTile;  // [128][BN] bf16
-  static constexpr int kPBytes = 128 * BN * 2;
-  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kBytes = kBar + 256;
   // One CTA per SM: TMEM (512 columns) is allocated whole.
   static constexpr int kSmemRequest = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
@@ -63,31 +70,39 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[2], v_full[2];
   uint64_t k_empty[2], v_empty[2];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_full;
-  uint64_t drain;
+  uint64_t s_full[2];  // per query tile
+  uint64_t p_full[2];  // per query tile
+  uint64_t o_done;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-struct TileCtx {
-  int64_t pq_lo, pq_hi;             // positions of the first / last valid query rows
+// Visibility bounds of a span of query rows (for tile classification).
+struct SpanCtx {
+  int64_t pq_lo, pq_hi;                // positions of the first / last valid query rows
   int64_t st_lo, st_hi, en_lo, en_hi;  // document [start, end) of pq_lo and pq_hi
-  int causal, docs;
 };
 
 struct KvTile {
   int32_t k_row;
   int32_t nk;
-  int64_t pk_lo;
+  int64_t pk_lo, pk_hi;
   int32_t kstride;
-  int32_t full;
 };
 
-// Next key/value tile of the group with any visible pair.  Identical in every role.
-__device__ __forceinline__ bool next_tile(const Schedule& s, const TileCtx& c, int seg_end,
-                                          int& seg, int& j0, KvTile& t) {
+__device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t pq_lo, int64_t pq_hi) {
+  c.pq_lo = pq_lo;
+  c.pq_hi = pq_hi;
+  c.st_lo = c.st_hi = c.en_lo = c.en_hi = 0;
+  if (a.cu_seqlens) {
+    doc_bounds(a.cu_seqlens, a.n_docs, pq_lo, &c.st_lo, &c.en_lo);
+    doc_bounds(a.cu_seqlens, a.n_docs, pq_hi, &c.st_hi, &c.en_hi);
+  }
+}
+
+// Next key/value tile with any visible pair for the CTA's query span.  Identical in every role.
+__device__ __forceinline__ bool next_tile(const Schedule& s, const SpanCtx& c, int causal, int docs,
+                                          int seg_end, int& seg, int& j0, KvTile& t) {
   while (seg < seg_end) {
     const int32_t k_row0 = s.s[seg].k_row0, nk_seg = s.s[seg].nk;
     const int32_t poff = s.s[seg].pos_off, pst = s.s[seg].pos_stride;
@@ -101,21 +116,26 @@ __device__ __forceinline__ bool next_tile(const Schedule& s, const TileCtx& c, i
     const int64_t pk_hi = pk_lo + (int64_t)pst * (nk - 1);
     const int jcur = j0;
     j0 += BN;
-    if ((c.causal && pk_lo > c.pq_hi) || (c.docs && pk_lo >= c.en_hi)) {
+    if ((causal && pk_lo > c.pq_hi) || (docs && pk_lo >= c.en_hi)) {
       ++seg;  // this and every later tile of the segment lie after the queries
       j0 = 0;
       continue;
     }
-    if (c.docs && pk_hi < c.st_lo) continue;  // before the first query's document
+    if (docs && pk_hi < c.st_lo) continue;  // before the first query's document
     t.k_row = k_row0 + jcur;
     t.nk = nk;
     t.pk_lo = pk_lo;
+    t.pk_hi = pk_hi;
     t.kstride = pst;
-    t.full = (nk == BN) && (!c.causal || pk_hi <= c.pq_lo) &&
-             (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo));
     return true;
   }
   return false;
+}
+
+// Every (row, key) pair of the tile visible for this query span (no mask needed)?
+__device__ __forceinline__ bool tile_full(const SpanCtx& c, const KvTile& t, int causal, int docs) {
+  return (t.nk == BN) && (!causal || t.pk_hi <= c.pq_lo) &&
+         (!docs || (t.pk_lo >= c.st_hi && t.pk_hi < c.en_lo));
 }
 
 template <int D>
@@ -145,23 +165,21 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int g, tile, h;
-  decode_unit(s, BM, a.Hq, blockIdx.x, &g, &tile, &h);
+  decode_unit(s, kRowsPerCta, a.Hq, blockIdx.x, &g, &tile, &h);
   const int hk = h / (a.Hq / a.Hkv);
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
   const int32_t qpos_off = s.g[g].pos_off, qpos_st = s.g[g].pos_stride;
   const int seg_begin = s.g[g].seg_begin, seg_end = seg_begin + s.g[g].seg_count;
-  const int i0 = tile * BM;
-  const int nq_tile = min(BM, nq - i0);
+  const int i0 = tile * kRowsPerCta;
+  const int nq0 = min(BM, nq - i0);
+  const int nq1 = max(0, min(BM, nq - i0 - BM));
+  const bool has1 = nq1 > 0;
+  const int causal = a.causal, docs = a.cu_seqlens != nullptr;
 
-  TileCtx c;
-  c.causal = a.causal;
-  c.docs = a.cu_seqlens != nullptr;
-  c.pq_lo = (int64_t)qpos_off + (int64_t)qpos_st * i0;
-  c.pq_hi = c.pq_lo + (int64_t)qpos_st * (nq_tile - 1);
-  c.st_lo = c.st_hi = c.en_lo = c.en_hi = 0;
-  if (c.docs) {
-    doc_bounds(a.cu_seqlens, a.n_docs, c.pq_lo, &c.st_lo, &c.en_lo);
-    doc_bounds(a.cu_seqlens, a.n_docs, c.pq_hi, &c.st_hi, &c.en_hi);
+  SpanCtx cta;  // both query tiles together
+  {
+    const int64_t lo = (int64_t)qpos_off + (int64_t)qpos_st * i0;
+    span_init(cta, a, lo, lo + (int64_t)qpos_st * (nq0 + nq1 - 1));
   }
 
   if (threadIdx.x == 0) {
@@ -172,18 +190,17 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       ptx::mbar_init(&bars->k_empty[i], 1);
       ptx::mbar_init(&bars->v_empty[i], 1);
       ptx::mbar_init(&bars->s_full[i], 1);
+      ptx::mbar_init(&bars->p_full[i], 128);
     }
-    ptx::mbar_init(&bars->p_full, 128);
-    ptx::mbar_init(&bars->o_full, 1);
-    ptx::mbar_init(&bars->drain, 1);
+    ptx::mbar_init(&bars->o_done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
@@ -193,19 +210,21 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
-
-  if (warp == 0) {
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<kRegsLow>();
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&bars->q_full, L::kTile);
+      ptx::mbar_arrive_expect_tx(&bars->q_full, (has1 ? 2 : 1) * L::kTile);
+      for (int w = 0; w < (has1 ? 2 : 1); ++w)
 #pragma unroll
-      for (int r = 0; r < D / 64; ++r)
-        ptx::tma_load_2d(smem + L::kQ + r * 16384, &tm_q, &bars->q_full, h * D + r * 64,
-                         q_row0 + i0);
+        for (int r = 0; r < D / 64; ++r)
+          ptx::tma_load_2d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
+                           h * D + r * 64, q_row0 + i0 + w * BM);
       int seg = seg_begin, j0 = 0, j = 0;
       KvTile t;
-      int issued[2] = {0, 0};
-      while (!*abort_flag && next_tile(s, c, seg_end, seg, j0, t)) {
+      int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
+      while (!*abort_flag && next_tile(s, cta, causal, docs, seg_end, seg, j0, t)) {
         const int st = j & 1;
         if (j >= 2 && !ptx::mbar_wait_bounded(&bars->k_empty[st], ((j >> 1) - 1) & 1, abort_flag,
                                               a.err, kWaitNs))
@@ -215,248 +234,277 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
         for (int r = 0; r < D / 64; ++r)
           ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->k_full[st],
                            hk * D + r * 64, t.k_row);
+        issued_k[st] = j + 1;
         if (j >= 2 && !ptx::mbar_wait_bounded(&bars->v_empty[st], ((j >> 1) - 1) & 1, abort_flag,
-                                              a.err, kWaitNs)) {
-          issued[st] = j + 1;
+                                              a.err, kWaitNs))
           break;
-        }
         ptx::mbar_arrive_expect_tx(&bars->v_full[st], L::kTile);
 #pragma unroll
         for (int r = 0; r < D / 64; ++r)
           ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->v_full[st],
                            hk * D + r * 64, t.k_row);
-        issued[st] = j + 1;
+        issued_v[st] = j + 1;
         ++j;
       }
       if (*abort_flag) {
         // drain: wait (bounded) for this CTA's own copies still in flight
         (void)ptx::mbar_wait_bounded(&bars->q_full, 0, nullptr, nullptr, kDrainNs);
-        for (int st = 0; st < 2; ++st)
-          if (issued[st] > 0) {
-            const uint32_t par = ((issued[st] - 1) >> 1) & 1;
-            (void)ptx::mbar_wait_bounded(&bars->k_full[st], par, nullptr, nullptr, kDrainNs);
-            (void)ptx::mbar_wait_bounded(&bars->v_full[st], par, nullptr, nullptr, kDrainNs);
-          }
+        for (int st = 0; st < 2; ++st) {
+          if (issued_k[st] > 0)
+            (void)ptx::mbar_wait_bounded(&bars->k_full[st], ((issued_k[st] - 1) >> 1) & 1, nullptr,
+                                         nullptr, kDrainNs);
+          if (issued_v[st] > 0)
+            (void)ptx::mbar_wait_bounded(&bars->v_full[st], ((issued_v[st] - 1) >> 1) & 1, nullptr,
+                                         nullptr, kDrainNs);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, 0, 1);
-      const uint32_t q_addr = sbase + L::kQ, p_addr = sbase + L::kP;
-      const uint32_t o_tmem = tmem + 256;
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, 0, 1);  // V is MN-major
+      auto qk = [&](int w, int st) {
+        const uint32_t q_addr = sbase + L::kQ + w * L::kTile;
+        const uint32_t k_addr = sbase + L::kK + st * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + w * 256, desc_kmajor<D>(q_addr, kk), desc_kmajor<D>(k_addr, kk),
+                           idesc_qk, kk > 0);
+      };
+      auto pv = [&](int w, int st, bool acc) {
+        const uint32_t v_addr = sbase + L::kV + st * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // P: 16 keys = 8 TMEM columns per step
+          ptx::mma_bf16_ts(tmem + w * 256 + 128, tmem + w * 256 + kk * 8,
+                           desc_v_mnmajor<D>(v_addr, kk), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = ptx::mbar_wait_bounded(&bars->q_full, 0, abort_flag, a.err, kWaitNs);
       bool any = false;
-      if (ptx::mbar_wait_bounded(&bars->q_full, 0, abort_flag, a.err, kWaitNs)) {
+      if (ok) {
         int seg = seg_begin, j0 = 0, j = 0;
         KvTile t;
-        bool more = next_tile(s, c, seg_end, seg, j0, t);
+        bool more = next_tile(s, cta, causal, docs, seg_end, seg, j0, t);
         while (true) {
-          if (more) {  // S(j) = Q K(j)^T
-            const int st = j & 1;
-            if (!ptx::mbar_wait_bounded(&bars->k_full[st], (j >> 1) & 1, abort_flag, a.err, kWaitNs))
-              break;
+          const int st = j & 1;
+          if (more) {  // S0 = Q0 K_j^T
+            if (!ptx::mbar_wait_bounded(&bars->k_full[st], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
             ptx::tc_fence_after();
-            const uint32_t k_addr = sbase + L::kK + st * L::kTile;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + st * 128, desc_kmajor<D>(q_addr, kk), desc_kmajor<D>(k_addr, kk),
-                               idesc_qk, kk > 0);
-            ptx::tc_commit(&bars->s_full[st]);
-            ptx::tc_commit(&bars->k_empty[st]);
+            qk(0, st);
+            ptx::tc_commit(&bars->s_full[0]);
             any = true;
           }
-          if (j >= 1) {  // O += P(j-1) V(j-1)
-            const int jp = j - 1, st = jp & 1;
-            if (!ptx::mbar_wait_bounded(&bars->p_full, jp & 1, abort_flag, a.err, kWaitNs)) break;
-            if (!ptx::mbar_wait_bounded(&bars->v_full[st], (jp >> 1) & 1, abort_flag, a.err, kWaitNs))
-              break;
+          if (has1 && j >= 1) {  // O1 += P1 V_{j-1}
+            const int jp = j - 1, stp = jp & 1;
+            if (!ptx::mbar_wait_bounded(&bars->p_full[1], jp & 1, abort_flag, a.err, kWaitNs)) break;
+            if (!ptx::mbar_wait_bounded(&bars->v_full[stp], (jp >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
             ptx::tc_fence_after();
-            const uint32_t v_addr = sbase + L::kV + st * L::kTile;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              ptx::mma_bf16_ss(o_tmem, desc_kmajor<D>(p_addr, kk), desc_v_mnmajor<D>(v_addr, kk),
-                               idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            ptx::tc_commit(&bars->o_full);
-            ptx::tc_commit(&bars->v_empty[st]);
+            pv(1, stp, jp > 0);
+            ptx::tc_commit(&bars->v_empty[stp]);
+          }
+          if (more) {
+            if (has1) {  // S1 = Q1 K_j^T
+              qk(1, st);
+              ptx::tc_commit(&bars->s_full[1]);
+            }
+            ptx::tc_commit(&bars->k_empty[st]);
+            // O0 += P0 V_j
+            if (!ptx::mbar_wait_bounded(&bars->p_full[0], j & 1, abort_flag, a.err, kWaitNs)) break;
+            if (!ptx::mbar_wait_bounded(&bars->v_full[st], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
+            ptx::tc_fence_after();
+            pv(0, st, j > 0);
+            if (!has1) ptx::tc_commit(&bars->v_empty[st]);
           }
           if (!more) break;
           ++j;
-          more = next_tile(s, c, seg_end, seg, j0, t);
+          more = next_tile(s, cta, causal, docs, seg_end, seg, j0, t);
         }
       }
-      if (any) {  // all MMAs of this CTA complete before TMEM is released
-        ptx::tc_commit(&bars->drain);
-        (void)ptx::mbar_wait_bounded(&bars->drain, 0, nullptr, a.err, kWaitNs);
+      // o_done: every MMA of this CTA has completed (also the TMEM release condition)
+      if (any) {
+        ptx::tc_commit(&bars->o_done);
+        (void)ptx::mbar_wait_bounded(&bars->o_done, 0, nullptr, a.err, kWaitNs);
+      } else {
+        ptx::mbar_arrive(&bars->o_done);
       }
     }
     __syncwarp();
+  }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
+    ptx::setmaxnreg_inc<kRegsHigh>();
+    // ------------------------------------------------------------ softmax warpgroups
+    const int w = warp >> 2;               // query tile of this warpgroup
     const int quad = warp & 3;             // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;        // query row within the tile
-    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-    const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
-    int64_t st_r = 0, en_r = 0;
-    if (c.docs && r < nq_tile) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
-    const float sl2 = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    int seg = seg_begin, j0 = 0, j = 0;
-    KvTile t;
-    uint8_t* prow = smem + L::kP + r * 128;
-    // Waits are made warp-uniform so the warp-collective tcgen05.ld/st and
-    // votes below always run converged.
-    auto wwait = [&](uint64_t* bar, uint32_t par) {
-      bool ok = ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
-      return __all_sync(0xffffffffu, ok);
-    };
-    while (__all_sync(0xffffffffu, *abort_flag == 0) && next_tile(s, c, seg_end, seg, j0, t)) {
-      const int st = j & 1;
-      if (!wwait(&bars->s_full[st], (j >> 1) & 1)) break;
-      ptx::tc_fence_after();
-      float sv[BN];
-      {
-        uint32_t rr[BN / 32][32];
-#pragma unroll
-        for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_ld32(lane_addr + st * 128 + ch * 32, rr[ch]);
-#pragma unroll
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          ptx::tmem_wait_ld_regs(rr[ch]);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[ch * 32 + i] = __uint_as_float(rr[ch][i]);
-        }
-      }
-      if (!t.full) {
-        int64_t hi = t.nk - 1, lo = 0;
-        if (c.causal) {
-          const int64_t d = pq - t.pk_lo;
-          hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
-        }
-        if (c.docs) {
-          const int64_t da = st_r - t.pk_lo;
-          lo = max(lo, da <= 0 ? (int64_t)0 : (da + t.kstride - 1) / t.kstride);
-          const int64_t db = en_r - 1 - t.pk_lo;
-          hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
-        }
-        const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
-#pragma unroll
-        for (int i = 0; i < BN; ++i) sv[i] = (i >= ilo && i <= ihi) ? sv[i] : -INFINITY;
-      }
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
-#pragma unroll
-      for (int i = 4; i < BN; i += 4) {
-        mx0 = fmaxf(mx0, sv[i]);
-        mx1 = fmaxf(mx1, sv[i + 1]);
-        mx2 = fmaxf(mx2, sv[i + 2]);
-        mx3 = fmaxf(mx3, sv[i + 3]);
-      }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = fmaxf(m, mt);
-      const bool need = m_new > m + kRescaleThreshold;
-      const bool warp_need = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (warp_need) {
-        alpha = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - m_new);
-        if (m_new != -INFINITY) m = m_new;
-        l *= alpha;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float l0 = 0.f, l1 = 0.f;
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int i = 0; i < BN; i += 2) {
-        const float p0 = ptx::ex2_approx(fmaf(sv[i], sl2, neg_m));
-        const float p1 = ptx::ex2_approx(fmaf(sv[i + 1], sl2, neg_m));
-        l0 += p0;
-        l1 += p1;
-        pk[i / 2] = ptx::pack_bf16x2(p0, p1);
-      }
-      l += l0 + l1;
-      // P and O are free once the previous P V has completed.
-      if (j > 0) {
-        if (!wwait(&bars->o_full, (j - 1) & 1)) break;
-        ptx::tc_fence_after();
-        if (warp_need) {
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t rr[32];
-            ptx::tmem_ld32(lane_addr + 256 + ch * 32, rr);
-            ptx::tmem_wait_ld_regs(rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            ptx::tmem_st32(lane_addr + 256 + ch * 32, rr);
+    const int nq_w = w == 0 ? nq0 : nq1;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + w * 256;
+    if (w == 0 || has1) {
+      SpanCtx mine;
+      const int64_t pq_lo_w = cta.pq_lo + (int64_t)qpos_st * (w * BM);
+      span_init(mine, a, pq_lo_w, pq_lo_w + (int64_t)qpos_st * (nq_w - 1));
+      const int64_t pq = pq_lo_w + (int64_t)qpos_st * r;
+      int64_t st_r = 0, en_r = 0;
+      if (docs && r < nq_w) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
+      const float sl2 = a.scale_log2;
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+      float m = -INFINITY, l = 0.f;
+      int seg = seg_begin, j0 = 0, j = 0;
+      KvTile t;
+      auto wwait = [&](uint64_t* bar, uint32_t par) {
+        bool ok = ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
+        return __all_sync(0xffffffffu, ok);
+      };
+      while (__all_sync(0xffffffffu, *abort_flag == 0) &&
+             next_tile(s, cta, causal, docs, seg_end, seg, j0, t)) {
+        const bool full = tile_full(mine, t, causal, docs);
+        int ilo = 0, ihi = BN - 1;
+        if (!full) {
+          int64_t hi = t.nk - 1, lo = 0;
+          if (causal) {
+            const int64_t d = pq - t.pk_lo;
+            hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
           }
-          ptx::tmem_wait_st();
+          if (docs) {
+            const int64_t da = st_r - t.pk_lo;
+            lo = max(lo, da <= 0 ? (int64_t)0 : (da + t.kstride - 1) / t.kstride);
+            const int64_t db = en_r - 1 - t.pk_lo;
+            hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
+          }
+          ilo = (int)lo;
+          ihi = (int)max(hi, (int64_t)-1);
         }
+        if (!wwait(&bars->s_full[w], j & 1)) break;
+        ptx::tc_fence_after();
+        float sv[BN];
+        {
+          uint32_t rr[BN / 32][32];
+#pragma unroll
+          for (int ch = 0; ch < BN / 32; ++ch) ptx::tmem_ld32(lane_addr + ch * 32, rr[ch]);
+#pragma unroll
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            ptx::tmem_wait_ld_regs(rr[ch]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[ch * 32 + i] = __uint_as_float(rr[ch][i]);
+          }
+        }
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) sv[i] = (i >= ilo && i <= ihi) ? sv[i] : -INFINITY;
+        }
+        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int i = 4; i < BN; i += 8) {
+          mx[0] = ptx::fmax3(mx[0], sv[i], sv[i + 1]);
+          mx[1] = ptx::fmax3(mx[1], sv[i + 2], sv[i + 3]);
+          if (i + 7 < BN) {
+            mx[2] = ptx::fmax3(mx[2], sv[i + 4], sv[i + 5]);
+            mx[3] = ptx::fmax3(mx[3], sv[i + 6], sv[i + 7]);
+          }
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float m_new = fmaxf(m, mt);
+        const bool need = m_new > m + kRescaleThreshold;
+        const bool warp_need = __any_sync(0xffffffffu, need);
+        if (warp_need) {
+          const float alpha = (m == -INFINITY) ? 0.f : ptx::ex2_approx(m - m_new);
+          if (m_new != -INFINITY) m = m_new;
+          l *= alpha;
+          if (j > 0) {
+            // the previous P V of this tile completed before this tile's S (commit order)
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t rr[32];
+              ptx::tmem_ld32(lane_addr + 128 + ch * 32, rr);
+              ptx::tmem_wait_ld_regs(rr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+              ptx::tmem_st32(lane_addr + 128 + ch * 32, rr);
+            }
+          }
+        }
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+        uint64_t lsum[4] = {ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f), ptx::f2_pack(0.f, 0.f),
+                            ptx::f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = half * 64 + 2 * i;
+            float x0, x1;
+            ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(sv[c], sv[c + 1]), sl2x2, nm2), x0, x1);
+            const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+            lsum[i & 3] = ptx::fadd2(lsum[i & 3], ptx::f2_pack(p0, p1));
+            pk[i] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st32(lane_addr + half * 32, pk);  // P over the first 64 columns of S
+        }
+        const uint64_t lsum2 = ptx::fadd2(ptx::fadd2(lsum[0], lsum[1]), ptx::fadd2(lsum[2], lsum[3]));
+        float ls0, ls1;
+        ptx::f2_unpack(lsum2, ls0, ls1);
+        l += ls0 + ls1;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->p_full[w]);
+        ++j;
       }
+      // ------------------------------------------------------------ epilogue
+      bool ok = __all_sync(0xffffffffu, *abort_flag == 0);
+      if (ok) ok = wwait(&bars->o_done, 0);
+      if (ok) {
+        ptx::tc_fence_after();
+        const bool valid = r < nq_w;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const int64_t orow = (int64_t)(s.g[g].o_row0 + i0 + w * BM + r) * a.o_ld + (int64_t)h * D;
 #pragma unroll
-      for (int cc = 0; cc < BN / 8; ++cc) {
-        uint8_t* dst = prow + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4(pk[cc * 4 + 0], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->p_full);
-      ++j;
-    }
-    // ------------------------------------------------------------ epilogue
-    bool ok = __all_sync(0xffffffffu, *abort_flag == 0);
-    if (ok && j > 0) {
-      ok = wwait(&bars->o_full, (j - 1) & 1);
-      ptx::tc_fence_after();
-    }
-    if (ok) {
-      const bool valid = r < nq_tile;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const int64_t orow = (int64_t)(s.g[g].o_row0 + i0 + r) * a.o_ld + (int64_t)h * D;
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t rr[32];
+          if (j > 0) {
+            ptx::tmem_ld32(lane_addr + 128 + ch * 32, rr);
+            ptx::tmem_wait_ld_regs(rr);
+          } else {
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t rr[32];
-        if (j > 0) {
-          ptx::tmem_ld32(lane_addr + 256 + ch * 32, rr);
-          ptx::tmem_wait_ld_regs(rr);
-        } else {
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;
+          }
+          if (valid) {
+            if (kOutF32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + ch * 32);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * inv_l,
+                                      __uint_as_float(rr[4 * v4 + 1]) * inv_l,
+                                      __uint_as_float(rr[4 * v4 + 2]) * inv_l,
+                                      __uint_as_float(rr[4 * v4 + 3]) * inv_l);
+            } else {
+              uint4* dst =
+                  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + ch * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4] = make_uint4(
+                    ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 0]) * inv_l,
+                                     __uint_as_float(rr[8 * v4 + 1]) * inv_l),
+                    ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 2]) * inv_l,
+                                     __uint_as_float(rr[8 * v4 + 3]) * inv_l),
+                    ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 4]) * inv_l,
+                                     __uint_as_float(rr[8 * v4 + 5]) * inv_l),
+                    ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 6]) * inv_l,
+                                     __uint_as_float(rr[8 * v4 + 7]) * inv_l));
+            }
+          }
         }
         if (valid) {
-          if (kOutF32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + ch * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(__uint_as_float(rr[4 * v4]) * inv_l,
-                                    __uint_as_float(rr[4 * v4 + 1]) * inv_l,
-                                    __uint_as_float(rr[4 * v4 + 2]) * inv_l,
-                                    __uint_as_float(rr[4 * v4 + 3]) * inv_l);
-          } else {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + ch * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(
-                  ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 0]) * inv_l,
-                                   __uint_as_float(rr[8 * v4 + 1]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 2]) * inv_l,
-                                   __uint_as_float(rr[8 * v4 + 3]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 4]) * inv_l,
-                                   __uint_as_float(rr[8 * v4 + 5]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 6]) * inv_l,
-                                   __uint_as_float(rr[8 * v4 + 7]) * inv_l));
-          }
+          const float Lr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+          a.lse[(int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + w * BM + r] = Lr;
         }
-      }
-      if (valid) {
-        const float L = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-        a.lse[(int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + r] = L;
       }
     }
     ptx::tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -510,8 +558,17 @@ cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, co
                        const CUtensorMap& mv, int64_t units, cudaStream_t st) {
   using L = Layout<D>;
   auto kern = attn_fwd_tc_kernel<D, kOutF32>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kSmemRequest);
+  // setmaxnreg.inc waits until the registers it asks for are free in the block's
+  // launch budget, so launch only if the split fits that budget.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return cuda_check(e, "cudaFuncGetAttributes(attn_fwd_tc)");
+  if ((int64_t)fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) {
+    set_last_error("attn_fwd_tc compiled with " + std::to_string(fa.numRegs) +
+                   " registers per thread, too few for its warpgroup register split");
+    return CP_ERR_UNSUPPORTED;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_fwd_tc)");
   kern<<<(unsigned)units, kThreads, L::kSmemRequest, st>>>(a, s, mq, mk, mv);
   return cuda_check(cudaGetLastError(), "attn_fwd_tc_kernel launch");
@@ -521,7 +578,7 @@ cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, co
 
 cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
                              cudaStream_t st) {
-  int64_t units = schedule_units(s, BM, a.Hq);
+  int64_t units = schedule_units(s, kRowsPerCta, a.Hq);
   if (units == 0) return CP_OK;
   if (units > 0x7fffffff) {
     set_last_error("too many query tiles for one launch");
