@@ -30,7 +30,8 @@
 //
 // This recomputes S and dP once more than a single fused kernel (7 instead of
 // 5 matrix products) in exchange for no fp32 atomic traffic on dQ.
-// Warps: 0 TMA producer, 1 MMA issuer (one thread), 2..5 softmax/epilogue.
+// Warps: 0..7 softmax/epilogue (warps w and w+4 share TMEM lane quadrant w and
+// split each row's columns), 8 TMA producer, 9 MMA issuer (one thread).
 // Every mbarrier wait is bounded (as in the forward kernel).
 #include <cuda.h>
 
@@ -43,7 +44,10 @@ namespace cpa {
 namespace {
 
 constexpr int D = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;       // warps 0..7 softmax (two per TMEM lane quadrant), 8 TMA, 9 MMA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -186,17 +190,17 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       ptx::mbar_init(&bars->q_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) ptx::mbar_init(&bars->s_full[i], 1);
-    ptx::mbar_init(&bars->p_full, 128);
+    ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
     ptx::mbar_init(&bars->pds_empty, 1);
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_do);
     ptx::prefetch_tensormap(&tm_k);
@@ -208,7 +212,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (whole warp)
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kKV);
@@ -257,7 +261,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
                                        nullptr, kDrainNs);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, A_BQ, 0, 0);  // K Q^T, V dO^T
@@ -317,8 +321,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warpgroup (thread = key row)
+    // ------------------------------------------------------------ softmax warpgroups (thread = key row)
     const int quad = warp & 3;
+    const int cb = (warp >> 2) * 32;  // this warpgroup's 32 query columns of the 64
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const int64_t pk = c.pk_lo + (int64_t)s.g[g].pos_stride * r;
@@ -355,29 +360,25 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
       if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
-      ptx::tmem_wait_ld_regs(sr[0]);
-      ptx::tmem_wait_ld_regs(sr[1]);
-      ptx::tmem_wait_ld_regs(dr[0]);
-      ptx::tmem_wait_ld_regs(dr[1]);
+      uint32_t sr[32], dr[32];
+      ptx::tmem_ld32(lane_addr + b * 128 + cb, sr);
+      ptx::tmem_ld32(lane_addr + b * 128 + 64 + cb, dr);
+      ptx::tmem_wait_ld_regs(sr);
+      ptx::tmem_wait_ld_regs(dr);
       const float* lse_st = lse_all + st * 2 * A_BQ;
-      uint32_t pp[A_BQ / 2], dd[A_BQ / 2];
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int cc = 0; cc < A_BQ; cc += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cc);
-        const float4 d4 = *reinterpret_cast<const float4*>(lse_st + A_BQ + cc);
+      for (int cc = 0; cc < 32; cc += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cb + cc);
+        const float4 d4 = *reinterpret_cast<const float4*>(lse_st + A_BQ + cb + cc);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
         const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
         float p[4], ds[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int col = cc + u;
-          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
+          const int col = cb + cc + u;
+          const float sv = __uint_as_float(sr[cc + u]);
+          const float dp = __uint_as_float(dr[cc + u]);
           p[u] = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lv[u])) : 0.f;
           ds[u] = p[u] * (dp - dl[u]);
         }
@@ -389,10 +390,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       // P^T / dS^T buffer is free once the previous tile's dV/dK products completed
       if (j > 0 && !wait_all(&bars->pds_empty, (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
 #pragma unroll
-      for (int ch = 0; ch < A_BQ / 8; ++ch) {
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int ch = (cb >> 3) + q4;  // 16-byte chunk (8 columns) of the 128-byte row
         const int off = ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2], pp[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(drow + off) = make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+        *reinterpret_cast<uint4*>(drow + off) = make_uint4(dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -406,8 +408,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       ptx::tc_fence_after();
       const bool valid = r < nk_tile;
       const int64_t krow = (int64_t)(k_row0 + r) * a.k_ld + (int64_t)hk * D;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = warp >> 2;  // warpgroup 0 stores dV, warpgroup 1 stores dK
         float* dst = (which == 0 ? a.dv_acc : a.dk_acc) + krow;
         const float mul = which == 0 ? 1.f : a.scale;
         const uint32_t col0 = which == 0 ? 256 : 384;
@@ -435,7 +437,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -559,18 +561,18 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars->s_full[i], 1);
-      ptx::mbar_init(&bars->ds_full[i], 128);
+      ptx::mbar_init(&bars->ds_full[i], kSoftmaxThreads);
       ptx::mbar_init(&bars->ds_empty[i], 1);
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_do);
     ptx::prefetch_tensormap(&tm_k);
@@ -582,7 +584,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * L::kQT);
@@ -620,7 +622,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16_f32(B_BQ, B_BN, 0, 0);  // Q K^T, dO V^T
@@ -678,8 +680,9 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warpgroup (thread = query row)
+    // ------------------------------------------------------------ softmax warpgroups (thread = query row)
     const int quad = warp & 3;
+    const int cb = (warp >> 2) * 32;  // this warpgroup's 32 key columns of the 64
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
@@ -715,24 +718,20 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
       if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
-      ptx::tmem_wait_ld_regs(sr[0]);
-      ptx::tmem_wait_ld_regs(sr[1]);
-      ptx::tmem_wait_ld_regs(dr[0]);
-      ptx::tmem_wait_ld_regs(dr[1]);
-      uint32_t dd[B_BN / 2];
+      uint32_t sr[32], dr[32];
+      ptx::tmem_ld32(lane_addr + b * 128 + cb, sr);
+      ptx::tmem_ld32(lane_addr + b * 128 + 64 + cb, dr);
+      ptx::tmem_wait_ld_regs(sr);
+      ptx::tmem_wait_ld_regs(dr);
+      uint32_t dd[16];
 #pragma unroll
-      for (int cc = 0; cc < B_BN; cc += 2) {
+      for (int cc = 0; cc < 32; cc += 2) {
         float ds[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int col = cc + u;
-          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
+          const int col = cb + cc + u;
+          const float sv = __uint_as_float(sr[cc + u]);
+          const float dp = __uint_as_float(dr[cc + u]);
           const float p = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lse2)) : 0.f;
           ds[u] = p * (dp - delta);
         }
@@ -742,9 +741,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       if (j >= 2 && !wait_all(&bars->ds_empty[b], ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
       uint8_t* drow = smem + L::kDS + b * L::kDSBytes + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < B_BN / 8; ++ch)
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int ch = (cb >> 3) + q4;
         *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
-            make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
+            make_uint4(dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
+      }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->ds_full[b]);
@@ -757,7 +758,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       ptx::tc_fence_after();
       float* dst = a.dq_acc + (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = (warp >> 2) * 2; ch < (warp >> 2) * 2 + 2; ++ch) {  // 64 columns per warpgroup
         uint32_t rr[32];
         if (j > 0) {
           ptx::tmem_ld32(lane_addr + 256 + ch * 32, rr);
@@ -779,7 +780,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
