@@ -235,6 +235,46 @@ def bench_ours(args):
     launches_per_step = 6
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
+    def timed(fn, reps):
+        """Mean device time (ms) of fn over reps, L2 flushed before each rep."""
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+            ts.append((a_, b_))
+        torch.cuda.synchronize()
+        return statistics.mean(x.elapsed_time(y) for x, y in ts)
+
+    def hbm_parts(reps):
+        """GB/s of the HBM-bound kernels on their workload shapes (algorithmic bytes:
+        every byte read once and written once)."""
+        out = {}
+        # LSE merge in fp32 at the ring shape (the stepwise ring's accumulator update)
+        o1 = torch.randn(S, H, D, device=dev)
+        o2 = torch.randn(S, H, D, device=dev)
+        l1 = torch.randn(H, S, device=dev)
+        l2 = torch.randn(H, S, device=dev)
+        ms = timed(lambda: cpa.cp_lse_merge(o1, l1, o2, l2, out=o1, lse=l1), reps)
+        nbytes = 3 * o1.numel() * 4 + 3 * l1.numel() * 4
+        out["lse_merge_f32_s8192_h32_d128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
+        del o1, o2, l1, l2
+        # Ulysses seq2head + head2seq at S=32768, H=32, D=128, P=16 (bf16)
+        Su, Pu = 32768, 16
+        x = torch.randn(Su, H, D, device=dev).to(torch.bfloat16)
+        y = torch.empty(Pu, Su, H // Pu, D, dtype=torch.bfloat16, device=dev)
+        ms1 = timed(lambda: cpa.cp_ulysses_seq2head(x, Pu, y=y), reps)
+        ms2 = timed(lambda: cpa.cp_ulysses_head2seq(y, Pu, x=x), reps)
+        nbytes = 2 * x.numel() * 2
+        out["ulysses_seq2head_s32768_h32_d128_p16"] = {"ms": ms1, "gbs": nbytes / (ms1 * 1e-3) / 1e9, "bytes": nbytes}
+        out["ulysses_head2seq_s32768_h32_d128_p16"] = {"ms": ms2, "gbs": nbytes / (ms2 * 1e-3) / 1e9, "bytes": nbytes}
+        del x, y
+        return out
+
     def gqa_fwd_bwd(n_steps):
         """fwd and fwd+bwd of the GQA ring workload (S=65536, Hq=32, Hkv=8, D=128,
         P=4, zigzag) through the public drivers, device-resident inputs."""
@@ -300,6 +340,7 @@ def bench_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     fb = gqa_fwd_bwd(args.fwd_bwd_steps) if args.fwd_bwd_steps > 0 else None
+    hbm = hbm_parts(max(5, min(args.steps, 20)))
     sampler.mark_end()
     clocks = sampler.finish()
     st = cpa.cp_check_device_status()
@@ -376,6 +417,7 @@ def bench_ours(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "attn_fwd_tc (ring, fused)", "peak_source": peaks["source"] + " burst bf16"},
             "fwd_bwd": None if fb is None else dict(fb, frac_of_peak=fb["fwd_bwd_tflops"] / peak),
+            "hbm_kernels": {k: dict(v, frac_of_hbm=v["gbs"] / peaks["hbm_gbs"]) for k, v in hbm.items()},
             "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,
                       "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
                       "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},

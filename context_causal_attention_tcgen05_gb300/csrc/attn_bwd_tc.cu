@@ -15,8 +15,11 @@
 //   that can see the keys (a key-major schedule: group = key run, segments =
 //   query runs).  Per query tile:
 //     S^T  = K Q^T, dP^T = V dO^T  -> TMEM, double-buffered (cols 0..255)
-//     softmax warps (thread = key row): P^T and dS^T (bf16) -> shared memory
-//     dV += P^T dO, dK += dS^T Q   -> TMEM accumulators (cols 256..511)
+//     softmax warps (thread = key row): P^T and dS^T (bf16) written back over
+//       the S^T / dP^T columns they came from
+//     dV += P^T dO, dK += dS^T Q   -> TMEM accumulators (cols 256..511), with
+//       P^T and dS^T as the TMEM A operand; issued after the NEXT tile's S^T so
+//       the softmax of one tile overlaps the products of its neighbours
 //   dK and dV are stored once at the end.  lse and Delta of each query tile
 //   are staged in shared memory by the producer warp with the Q/dO tiles.
 //
@@ -24,8 +27,9 @@
 //   walking every 64-key tile it sees (a query-major schedule, as in the
 //   forward).  Per key tile:
 //     S = Q K^T, dP = dO V^T       -> TMEM, double-buffered (cols 0..255)
-//     softmax warps (thread = query row): dS (bf16) -> shared memory
-//     dQ += dS K                   -> TMEM accumulator (cols 256..383)
+//     softmax warps (thread = query row): dS (bf16) written over the dP columns
+//     dQ += dS K                   -> TMEM accumulator (cols 256..383), dS as
+//       the TMEM A operand
 //   dQ is stored once at the end.
 //
 // This recomputes S and dP once more than a single fused kernel (7 instead of
@@ -81,9 +85,7 @@ struct ALayout {
   static constexpr int kV = kK + kKV;
   static constexpr int kQ = kV + kKV;            // A_QST stages
   static constexpr int kDO = kQ + A_QST * kQT;   // A_QST stages
-  static constexpr int kPT = kDO + A_QST * kQT;  // [128 keys][64 q] bf16
-  static constexpr int kDST = kPT + A_BK * A_BQ * 2;
-  static constexpr int kLse = kDST + A_BK * A_BQ * 2;  // A_QST x (64 lse*log2e, 64 Delta)
+  static constexpr int kLse = kDO + A_QST * kQT;  // A_QST x (64 lse*log2e, 64 Delta)
   static constexpr int kBar = kLse + A_QST * 2 * A_BQ * 4;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kSmemRequest = kBytes + 1024;
@@ -94,8 +96,7 @@ struct ABars {
   uint64_t q_full[A_QST], q_empty[A_QST];
   uint64_t s_full[2];
   uint64_t p_full;
-  uint64_t pds_empty;
-  uint64_t drain;
+  uint64_t done;  // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -191,8 +192,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) ptx::mbar_init(&bars->s_full[i], 1);
     ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
-    ptx::mbar_init(&bars->pds_empty, 1);
-    ptx::mbar_init(&bars->drain, 1);
+    ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -265,58 +265,61 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, A_BQ, 0, 0);  // K Q^T, V dO^T
-      constexpr uint32_t id_kv = ptx::idesc_bf16_f32(128, D, 0, 1);    // P^T dO, dS^T Q
+      constexpr uint32_t id_kv = ptx::idesc_bf16_f32(128, D, 0, 1);    // P^T dO, dS^T Q (TMEM A)
       const uint32_t k_addr = sbase + L::kK, v_addr = sbase + L::kV;
-      const uint32_t pt_addr = sbase + L::kPT, dst_addr = sbase + L::kDST;
-      bool any = false;
+      bool issued = false;
+      // S^T and dP^T of query tile jj into TMEM buffer jj & 1
+      auto issue_s = [&](int jj) -> bool {
+        const int st = jj % A_QST, b = jj & 1;
+        if (!ptx::mbar_wait_bounded(&bars->q_full[st], (jj / A_QST) & 1, abort_flag, a.err, kWaitNs))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
+        const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + b * 128, desc_k(k_addr, kk, 16384), desc_k(q_addr, kk, 8192), id_s,
+                           kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + b * 128 + 64, desc_k(v_addr, kk, 16384), desc_k(do_addr, kk, 8192),
+                           id_s, kk > 0);
+        ptx::tc_commit(&bars->s_full[b]);
+        issued = true;
+        return true;
+      };
       if (ptx::mbar_wait_bounded(&bars->kv_full, 0, abort_flag, a.err, kWaitNs)) {
         int hh = 0, seg = seg_begin, i0 = 0, j = 0;
         QTile t;
-        bool more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
-        while (true) {
-          if (more) {
-            const int st = j % A_QST, b = j & 1;
-            if (!ptx::mbar_wait_bounded(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err, kWaitNs))
-              break;
-            ptx::tc_fence_after();
-            const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
-            const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
+        bool have = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+        if (have && !issue_s(0)) have = false;
+        while (have) {
+          const bool more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+          if (more && !issue_s(j + 1)) break;  // next tile's scores run during this softmax
+          if (!ptx::mbar_wait_bounded(&bars->p_full, j & 1, abort_flag, a.err, kWaitNs)) break;
+          ptx::tc_fence_after();
+          const int st = j % A_QST, b = j & 1;
+          const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
+          const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
+          // K step kk = 16 queries = 8 packed columns; queries 0..31 / 32..63 sit at column 0 / 32
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + b * 128, desc_k(k_addr, kk, 16384), desc_k(q_addr, kk, 8192), id_s,
-                               kk > 0);
+          for (int kk = 0; kk < A_BQ / 16; ++kk)
+            ptx::mma_bf16_ts(tmem + 256, tmem + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8,
+                             desc_mn(do_addr, kk, 8192), id_kv, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + b * 128 + 64, desc_k(v_addr, kk, 16384), desc_k(do_addr, kk, 8192),
-                               id_s, kk > 0);
-            ptx::tc_commit(&bars->s_full[b]);
-            any = true;
-          }
-          if (j >= 1) {
-            const int jp = j - 1, stp = jp % A_QST;
-            if (!ptx::mbar_wait_bounded(&bars->p_full, jp & 1, abort_flag, a.err, kWaitNs)) break;
-            ptx::tc_fence_after();
-            const uint32_t q_addr = sbase + L::kQ + stp * L::kQT;
-            const uint32_t do_addr = sbase + L::kDO + stp * L::kQT;
-#pragma unroll
-            for (int kk = 0; kk < A_BQ / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + 256, desc_k(pt_addr, kk, 16384), desc_mn(do_addr, kk, 8192), id_kv,
-                               (jp > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < A_BQ / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + 384, desc_k(dst_addr, kk, 16384), desc_mn(q_addr, kk, 8192), id_kv,
-                               (jp > 0 || kk > 0) ? 1u : 0u);
-            ptx::tc_commit(&bars->pds_empty);
-            ptx::tc_commit(&bars->q_empty[stp]);
-          }
-          if (!more) break;
+          for (int kk = 0; kk < A_BQ / 16; ++kk)
+            ptx::mma_bf16_ts(tmem + 384, tmem + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                             desc_mn(q_addr, kk, 8192), id_kv, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::tc_commit(&bars->q_empty[st]);
           ++j;
-          more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+          have = more;
         }
       }
-      if (any) {
-        ptx::tc_commit(&bars->drain);
-        (void)ptx::mbar_wait_bounded(&bars->drain, 0, nullptr, a.err, kWaitNs);
+      if (issued) {
+        ptx::tc_commit(&bars->done);
+        (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
+      } else {
+        ptx::mbar_arrive(&bars->done);
       }
     }
     __syncwarp();
@@ -333,8 +336,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     int hh = 0, seg = seg_begin, i0 = 0, j = 0;
     QTile t;
     bool ok = true;
-    uint8_t* prow = smem + L::kPT + r * 128;
-    uint8_t* drow = smem + L::kDST + r * 128;
     while (__all_sync(0xffffffffu, *abort_flag == 0) &&
            next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
       const int st = j % A_QST, b = j & 1;
@@ -387,23 +388,17 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
         dd[cc / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
       }
-      // P^T / dS^T buffer is free once the previous tile's dV/dK products completed
-      if (j > 0 && !wait_all(&bars->pds_empty, (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = (cb >> 3) + q4;  // 16-byte chunk (8 columns) of the 128-byte row
-        const int off = ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
-        *reinterpret_cast<uint4*>(drow + off) = make_uint4(dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
-      }
-      ptx::fence_proxy_async_smem();
+      // P^T and dS^T (two bf16 per column) over the S^T / dP^T columns this warpgroup read
+      ptx::tmem_st16(lane_addr + b * 128 + cb, pp);
+      ptx::tmem_st16(lane_addr + b * 128 + 64 + cb, dd);
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->p_full);
       ++j;
     }
     // ------------------------------------------------------------ dK / dV epilogue
     ok = ok && __all_sync(0xffffffffu, *abort_flag == 0);
-    if (ok && j > 0) ok = wait_all(&bars->pds_empty, (j - 1) & 1, abort_flag, a.err);
+    if (ok) ok = wait_all(&bars->done, 0, abort_flag, a.err);
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = r < nk_tile;
@@ -456,9 +451,7 @@ struct BLayout {
   static constexpr int kDO = kQ + kQT;
   static constexpr int kK = kDO + kQT;       // B_KST stages
   static constexpr int kV = kK + B_KST * kKT;
-  static constexpr int kDS = kV + B_KST * kKT;  // 2 x [128 q][64 keys] bf16
-  static constexpr int kDSBytes = B_BQ * B_BN * 2;
-  static constexpr int kBar = kDS + 2 * kDSBytes;
+  static constexpr int kBar = kV + B_KST * kKT;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kSmemRequest = kBytes + 1024;
 };
@@ -467,8 +460,8 @@ struct BBars {
   uint64_t q_full;
   uint64_t k_full[B_KST], v_full[B_KST], kv_empty[B_KST];
   uint64_t s_full[2];
-  uint64_t ds_full[2], ds_empty[2];
-  uint64_t drain;
+  uint64_t ds_full[2];
+  uint64_t done;  // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -562,9 +555,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars->s_full[i], 1);
       ptx::mbar_init(&bars->ds_full[i], kSoftmaxThreads);
-      ptx::mbar_init(&bars->ds_empty[i], 1);
     }
-    ptx::mbar_init(&bars->drain, 1);
+    ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -660,12 +652,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
               break;
             ptx::tc_fence_after();
             const uint32_t k_addr = sbase + L::kK + stp * L::kKT;
-            const uint32_t ds_addr = sbase + L::kDS + bp * L::kDSBytes;
+            // K step kk = 16 keys = 8 packed columns; keys 0..31 / 32..63 sit at column 64 / 96
 #pragma unroll
             for (int kk = 0; kk < B_BN / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + 256, desc_k(ds_addr, kk, 16384), desc_mn(k_addr, kk, 8192), id_q,
-                               (jp > 0 || kk > 0) ? 1u : 0u);
-            ptx::tc_commit(&bars->ds_empty[bp]);
+              ptx::mma_bf16_ts(tmem + 256, tmem + bp * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                               desc_mn(k_addr, kk, 8192), id_q, (jp > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(&bars->kv_empty[stp]);
           }
           if (!more) break;
@@ -674,8 +665,10 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         }
       }
       if (any) {
-        ptx::tc_commit(&bars->drain);
-        (void)ptx::mbar_wait_bounded(&bars->drain, 0, nullptr, a.err, kWaitNs);
+        ptx::tc_commit(&bars->done);
+        (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
+      } else {
+        ptx::mbar_arrive(&bars->done);
       }
     }
     __syncwarp();
@@ -737,23 +730,16 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         }
         dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
       }
-      // dS buffer b is free once the dQ product of tile j-2 completed
-      if (j >= 2 && !wait_all(&bars->ds_empty[b], ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-      uint8_t* drow = smem + L::kDS + b * L::kDSBytes + r * 128;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = (cb >> 3) + q4;
-        *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
-            make_uint4(dd[4 * q4], dd[4 * q4 + 1], dd[4 * q4 + 2], dd[4 * q4 + 3]);
-      }
-      ptx::fence_proxy_async_smem();
+      // dS (two bf16 per column) over the dP columns this warpgroup read
+      ptx::tmem_st16(lane_addr + b * 128 + 64 + cb, dd);
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->ds_full[b]);
       ++j;
     }
     // ------------------------------------------------------------ dQ epilogue
     ok = ok && __all_sync(0xffffffffu, *abort_flag == 0);
-    if (ok && j > 0) ok = wait_all(&bars->ds_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, a.err);
+    if (ok) ok = wait_all(&bars->done, 0, abort_flag, a.err);
     if (ok) {
       ptx::tc_fence_after();
       float* dst = a.dq_acc + (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
