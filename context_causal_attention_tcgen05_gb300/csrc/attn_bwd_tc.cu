@@ -34,8 +34,11 @@
 //
 // This recomputes S and dP once more than a single fused kernel (7 instead of
 // 5 matrix products) in exchange for no fp32 atomic traffic on dQ.
-// Warps: 0..7 softmax/epilogue (warps w and w+4 share TMEM lane quadrant w and
-// split each row's columns), 8 TMA producer, 9 MMA issuer (one thread).
+// Warps: 0..3 and 4..7 are two softmax warpgroups that take alternate tiles
+// (two independent MMA -> softmax -> MMA chains per CTA, so each hides the
+// other's hand-off latency), each with its own TMEM S/dP buffer; 8 TMA
+// producer, 9 MMA issuer (one thread); the third warpgroup gives registers to
+// the softmax ones (setmaxnreg).
 // Every mbarrier wait is bounded (as in the forward kernel).
 #include <cuda.h>
 
@@ -48,10 +51,14 @@ namespace cpa {
 namespace {
 
 constexpr int D = 128;
-constexpr int kThreads = 320;       // warps 0..7 softmax (two per TMEM lane quadrant), 8 TMA, 9 MMA
+constexpr int kThreads = 384;       // warps 0..7 softmax (two warpgroups), 8 TMA, 9 MMA, 10..11 spare
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kWgThreads = 128;
+// Register split (launch: 384 x 168 = 64512): the TMA/MMA warpgroup drops to 88, the
+// two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -95,7 +102,7 @@ struct ABars {
   uint64_t kv_full;
   uint64_t q_full[A_QST], q_empty[A_QST];
   uint64_t s_full[2];
-  uint64_t p_full;
+  uint64_t p_full[2];
   uint64_t done;  // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
@@ -190,8 +197,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       ptx::mbar_init(&bars->q_full[i], 2);  // TMA (expect_tx) + the warp's lse/Delta stores
       ptx::mbar_init(&bars->q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) ptx::mbar_init(&bars->s_full[i], 1);
-    ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->s_full[i], 1);
+      ptx::mbar_init(&bars->p_full[i], kWgThreads);
+    }
     ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -212,6 +221,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<kRegsLow>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (whole warp)
     if (lane == 0) {
@@ -289,30 +300,39 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         return true;
       };
       if (ptx::mbar_wait_bounded(&bars->kv_full, 0, abort_flag, a.err, kWaitNs)) {
-        int hh = 0, seg = seg_begin, i0 = 0, j = 0;
+        int hh = 0, seg = seg_begin, i0 = 0;
         QTile t;
-        bool have = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
-        if (have && !issue_s(0)) have = false;
-        while (have) {
-          const bool more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
-          if (more && !issue_s(j + 1)) break;  // next tile's scores run during this softmax
-          if (!ptx::mbar_wait_bounded(&bars->p_full, j & 1, abort_flag, a.err, kWaitNs)) break;
+        int found = 0;  // query tiles the iterator has produced so far
+        bool exhausted = false;
+        auto advance = [&]() {
+          if (!exhausted) {
+            if (next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) ++found;
+            else exhausted = true;
+          }
+        };
+        bool fail = false;
+        advance();
+        if (found > 0 && !issue_s(0)) fail = true;
+        advance();
+        if (!fail && found > 1 && !issue_s(1)) fail = true;
+        for (int j = 0; !fail && j < found; ++j) {
+          const int b = j & 1, st = j % A_QST;
+          if (!ptx::mbar_wait_bounded(&bars->p_full[b], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
           ptx::tc_fence_after();
-          const int st = j % A_QST, b = j & 1;
           const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
           const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
-          // K step kk = 16 queries = 8 packed columns; queries 0..31 / 32..63 sit at column 0 / 32
+          // P^T / dS^T: 64 queries packed two per column (K step kk = 8 columns)
 #pragma unroll
           for (int kk = 0; kk < A_BQ / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + 256, tmem + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8,
-                             desc_mn(do_addr, kk, 8192), id_kv, (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16_ts(tmem + 256, tmem + b * 128 + kk * 8, desc_mn(do_addr, kk, 8192), id_kv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < A_BQ / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + 384, tmem + b * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                             desc_mn(q_addr, kk, 8192), id_kv, (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16_ts(tmem + 384, tmem + b * 128 + 64 + kk * 8, desc_mn(q_addr, kk, 8192), id_kv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
           ptx::tc_commit(&bars->q_empty[st]);
-          ++j;
-          have = more;
+          advance();
+          if (found > j + 2 && !issue_s(j + 2)) break;  // reuses buffer b after these products
         }
       }
       if (issued) {
@@ -323,10 +343,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       }
     }
     __syncwarp();
+  }
   } else {
+    ptx::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax warpgroups (thread = key row)
     const int quad = warp & 3;
-    const int cb = (warp >> 2) * 32;  // this warpgroup's 32 query columns of the 64
+    const int w = warp >> 2;  // this warpgroup takes the query tiles j with j % 2 == w
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const int64_t pk = c.pk_lo + (int64_t)s.g[g].pos_stride * r;
@@ -338,7 +360,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     bool ok = true;
     while (__all_sync(0xffffffffu, *abort_flag == 0) &&
            next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
-      const int st = j % A_QST, b = j & 1;
+      if ((j & 1) != w) {
+        ++j;
+        continue;
+      }
+      const int st = j % A_QST, b = w;
       int64_t hi = t.nq - 1, lo = 0;  // visible query columns of this key row: [lo, hi]
       if (r >= nk_tile) {
         hi = -1;
@@ -361,25 +387,29 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
       if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[32], dr[32];
-      ptx::tmem_ld32(lane_addr + b * 128 + cb, sr);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64 + cb, dr);
-      ptx::tmem_wait_ld_regs(sr);
-      ptx::tmem_wait_ld_regs(dr);
+      uint32_t sr[2][32], dr[2][32];
+      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
+      ptx::tmem_wait_ld_regs(sr[0]);
+      ptx::tmem_wait_ld_regs(sr[1]);
+      ptx::tmem_wait_ld_regs(dr[0]);
+      ptx::tmem_wait_ld_regs(dr[1]);
       const float* lse_st = lse_all + st * 2 * A_BQ;
-      uint32_t pp[16], dd[16];
+      uint32_t pp[32], dd[32];
 #pragma unroll
-      for (int cc = 0; cc < 32; cc += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cb + cc);
-        const float4 d4 = *reinterpret_cast<const float4*>(lse_st + A_BQ + cb + cc);
+      for (int cc = 0; cc < A_BQ; cc += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cc);
+        const float4 d4 = *reinterpret_cast<const float4*>(lse_st + A_BQ + cc);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
         const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
         float p[4], ds[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int col = cb + cc + u;
-          const float sv = __uint_as_float(sr[cc + u]);
-          const float dp = __uint_as_float(dr[cc + u]);
+          const int col = cc + u;
+          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
+          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
           p[u] = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lv[u])) : 0.f;
           ds[u] = p[u] * (dp - dl[u]);
         }
@@ -388,12 +418,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
         dd[cc / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
       }
-      // P^T and dS^T (two bf16 per column) over the S^T / dP^T columns this warpgroup read
-      ptx::tmem_st16(lane_addr + b * 128 + cb, pp);
-      ptx::tmem_st16(lane_addr + b * 128 + 64 + cb, dd);
+      // P^T and dS^T (two bf16 per column) over the S^T / dP^T columns just read
+      ptx::tmem_st32(lane_addr + b * 128, pp);
+      ptx::tmem_st32(lane_addr + b * 128 + 64, dd);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->p_full);
+      ptx::mbar_arrive(&bars->p_full[b]);
       ++j;
     }
     // ------------------------------------------------------------ dK / dV epilogue
@@ -554,7 +584,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars->s_full[i], 1);
-      ptx::mbar_init(&bars->ds_full[i], kSoftmaxThreads);
+      ptx::mbar_init(&bars->ds_full[i], kWgThreads);
     }
     ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
@@ -576,6 +606,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<kRegsLow>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -652,11 +684,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
               break;
             ptx::tc_fence_after();
             const uint32_t k_addr = sbase + L::kK + stp * L::kKT;
-            // K step kk = 16 keys = 8 packed columns; keys 0..31 / 32..63 sit at column 64 / 96
+            // dS: 64 keys packed two per column over the dP columns (K step kk = 8 columns)
 #pragma unroll
             for (int kk = 0; kk < B_BN / 16; ++kk)
-              ptx::mma_bf16_ts(tmem + 256, tmem + bp * 128 + 64 + (kk >> 1) * 32 + (kk & 1) * 8,
-                               desc_mn(k_addr, kk, 8192), id_q, (jp > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_bf16_ts(tmem + 256, tmem + bp * 128 + 64 + kk * 8, desc_mn(k_addr, kk, 8192), id_q,
+                               (jp > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit(&bars->kv_empty[stp]);
           }
           if (!more) break;
@@ -672,10 +704,12 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       }
     }
     __syncwarp();
+  }
   } else {
+    ptx::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax warpgroups (thread = query row)
     const int quad = warp & 3;
-    const int cb = (warp >> 2) * 32;  // this warpgroup's 32 key columns of the 64
+    const int w = warp >> 2;  // this warpgroup takes the key tiles j with j % 2 == w
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
@@ -694,7 +728,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     KvTile t;
     bool ok = true;
     while (__all_sync(0xffffffffu, *abort_flag == 0) && next_ktile(s, c, seg_end, seg, j0, t)) {
-      const int b = j & 1;
+      if ((j & 1) != w) {
+        ++j;
+        continue;
+      }
+      const int b = w;
       int64_t hi = t.nk - 1, lo = 0;
       if (!t.full) {
         if (c.causal) {
@@ -711,27 +749,31 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
       if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[32], dr[32];
-      ptx::tmem_ld32(lane_addr + b * 128 + cb, sr);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64 + cb, dr);
-      ptx::tmem_wait_ld_regs(sr);
-      ptx::tmem_wait_ld_regs(dr);
-      uint32_t dd[16];
+      uint32_t sr[2][32], dr[2][32];
+      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
+      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
+      ptx::tmem_wait_ld_regs(sr[0]);
+      ptx::tmem_wait_ld_regs(sr[1]);
+      ptx::tmem_wait_ld_regs(dr[0]);
+      ptx::tmem_wait_ld_regs(dr[1]);
+      uint32_t dd[32];
 #pragma unroll
-      for (int cc = 0; cc < 32; cc += 2) {
+      for (int cc = 0; cc < B_BN; cc += 2) {
         float ds[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int col = cb + cc + u;
-          const float sv = __uint_as_float(sr[cc + u]);
-          const float dp = __uint_as_float(dr[cc + u]);
+          const int col = cc + u;
+          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
+          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
           const float p = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lse2)) : 0.f;
           ds[u] = p * (dp - delta);
         }
         dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
       }
-      // dS (two bf16 per column) over the dP columns this warpgroup read
-      ptx::tmem_st16(lane_addr + b * 128 + 64 + cb, dd);
+      // dS (two bf16 per column) over the dP columns just read
+      ptx::tmem_st32(lane_addr + b * 128 + 64, dd);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->ds_full[b]);
@@ -883,6 +925,18 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   if ((r = make_map(&mk64, a.k, k_rows, (int64_t)a.Hkv * D, B_BN)) != CP_OK) return r;
   if ((r = make_map(&mv64, a.v, k_rows, (int64_t)a.Hkv * D, B_BN)) != CP_OK) return r;
 
+  // setmaxnreg.inc waits until the registers it asks for are free in the block's launch
+  // budget, so launch only if each kernel's compiled register count covers the split.
+  for (const void* kfn : {(const void*)attn_bwd_dkdv_kernel, (const void*)attn_bwd_dq_kernel}) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kfn);
+    if (e != cudaSuccess) return cuda_check(e, "cudaFuncGetAttributes(attn_bwd)");
+    if ((int64_t)fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh) {
+      set_last_error("attention backward compiled with " + std::to_string(fa.numRegs) +
+                     " registers per thread, too few for its warpgroup register split");
+      return CP_ERR_UNSUPPORTED;
+    }
+  }
   // dK / dV over the key-major schedule
   int64_t units = schedule_units(s, A_BK, a.Hkv);
   if (units > 0) {
