@@ -8,38 +8,39 @@
 //   dS = P o (dP - Delta),   Delta = rowsum(dO o O),
 //   dQ = scale * dS K,       dK = scale * dS^T Q.
 //
-// Two kernels, neither uses atomics (gradients are deterministic):
+// Two kernels, neither uses atomics (gradients are deterministic).  Every
+// product is M=128 x N=128 per instruction: a tcgen05.mma costs about the same
+// time for N = 64 as for N = 128, so 64-wide tiles would halve the rate.
 //
-// attn_bwd_dkdv_kernel: one CTA = one 128-key tile of one key/value head,
-//   looping over the G query heads that read it and every 64-row query tile
-//   that can see the keys (a key-major schedule: group = key run, segments =
-//   query runs).  Per query tile:
-//     S^T  = K Q^T, dP^T = V dO^T  -> TMEM, double-buffered (cols 0..255)
-//     softmax warps (thread = key row): P^T and dS^T (bf16) written back over
-//       the S^T / dP^T columns they came from
-//     dV += P^T dO, dK += dS^T Q   -> TMEM accumulators (cols 256..511), with
-//       P^T and dS^T as the TMEM A operand; issued after the NEXT tile's S^T so
-//       the softmax of one tile overlaps the products of its neighbours
-//   dK and dV are stored once at the end.  lse and Delta of each query tile
-//   are staged in shared memory by the producer warp with the Q/dO tiles.
+// attn_bwd_dkdv_kernel: one CTA = one 128-key tile of one key/value head
+//   (K, V in shared memory), looping over the G query heads that read it and
+//   every 128-row query tile that can see the keys (a key-major schedule:
+//   group = key run, segments = query runs).  Per query tile j:
+//     S^T = K Q^T (TMEM 0..127), dP^T = V dO^T (TMEM 128..255)
+//     softmax warps (thread = key row, each warpgroup 64 of the query
+//       columns): phase 1 P^T from S^T as soon as S^T lands (written back
+//       over S^T, two bf16 per column); phase 2 dS^T once dP^T lands
+//     dV += P^T dO (TMEM 256..383), dK += dS^T Q (TMEM 384..511), P^T and dS^T
+//       as the TMEM A operand
+//   MMA issue order dV_j, S^T_{j+1}, dK_j, dP^T_{j+1}: the tensor pipe always
+//   has the next tile's scores queued while the softmax works.  lse and Delta
+//   of each query tile are staged with cp.async alongside the Q/dO tiles.
 //
-// attn_bwd_dq_kernel: one CTA = one 128-row query tile of one query head,
-//   walking every 64-key tile it sees (a query-major schedule, as in the
-//   forward).  Per key tile:
-//     S = Q K^T, dP = dO V^T       -> TMEM, double-buffered (cols 0..255)
-//     softmax warps (thread = query row): dS (bf16) written over the dP columns
-//     dQ += dS K                   -> TMEM accumulator (cols 256..383), dS as
-//       the TMEM A operand
-//   dQ is stored once at the end.
+// attn_bwd_dq_kernel: one CTA = one 128-row query tile of one query head.  The
+//   softmax warps copy Q and dO into TMEM once (A operands); the CTA walks
+//   every 128-key tile it sees (a query-major schedule, as in the forward):
+//     S = Q K^T (TMEM 0..127), dP = dO V^T (TMEM 128..255)
+//     softmax warps (thread = query row, each warpgroup 64 of the key columns):
+//       phase 1 P from S (then S is free for the next tile), phase 2 dS once
+//       dP lands, written over dP
+//     dQ += dS K (TMEM 256..383)
+//   MMA issue order S_{j+1}, dQ_j, dP_{j+1}.  Q, dO in TMEM 384..447, 448..511.
 //
 // This recomputes S and dP once more than a single fused kernel (7 instead of
 // 5 matrix products) in exchange for no fp32 atomic traffic on dQ.
-// Warps: 0..3 and 4..7 are two softmax warpgroups that take alternate tiles
-// (two independent MMA -> softmax -> MMA chains per CTA, so each hides the
-// other's hand-off latency), each with its own TMEM S/dP buffer; 8 TMA
-// producer, 9 MMA issuer (one thread); the third warpgroup gives registers to
-// the softmax ones (setmaxnreg).
-// Every mbarrier wait is bounded (as in the forward kernel).
+// Warps: 0..7 softmax (two warpgroups), 8 TMA producer, 9 MMA issuer (one
+// thread), 10..11 spare (the third warpgroup gives registers to the softmax
+// ones with setmaxnreg).  Every mbarrier wait is bounded (as in the forward).
 #include <cuda.h>
 
 #include <vector>
@@ -51,10 +52,10 @@ namespace cpa {
 namespace {
 
 constexpr int D = 128;
-constexpr int kThreads = 384;       // warps 0..7 softmax (two warpgroups), 8 TMA, 9 MMA, 10..11 spare
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kWgThreads = 128;
+constexpr int kSoftmaxThreads = 256;
 // Register split (launch: 384 x 168 = 64512): the TMA/MMA warpgroup drops to 88, the
 // two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
 constexpr int kRegsLow = 88;
@@ -63,14 +64,21 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTileRows = 128;
+constexpr int kTileBytes = kTileRows * D * 2;  // 32 KB: [128 rows][128 bf16], two 64-column regions
 
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk, uint32_t region_bytes) {
-  // K-major, 128B swizzle: K step of 16 bf16 = 32 bytes inside a 64-column region.
-  return ptx::smem_desc_sw128(base + (kk >> 2) * region_bytes + (kk & 3) * 32, 16, 1024);
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
+  // K-major, 128B swizzle: K step of 16 bf16 = 32 bytes inside a 64-column (16 KB) region.
+  return ptx::smem_desc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk, uint32_t lbo) {
-  // MN-major, 128B swizzle: K step of 16 rows of 128 bytes; next 64 MN columns at +lbo.
-  return ptx::smem_desc_sw128(base + kk * (16 * 128), lbo, 1024);
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
+  // MN-major, 128B swizzle: K step of 16 rows of 128 bytes; next 64 N columns at +16 KB.
+  return ptx::smem_desc_sw128(base + kk * (16 * 128), 16384, 1024);
+}
+// TMEM A operand of K = 128 packed over two 64-column halves written by the two
+// warpgroups: K step kk (16 values = 8 columns) of half kk / 4.
+__device__ __forceinline__ uint32_t a_split(uint32_t base, int kk) {
+  return base + (kk >> 2) * 64 + (kk & 3) * 8;
 }
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t par, volatile int* abort_flag,
@@ -79,21 +87,43 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t par, volatile i
   return __all_sync(0xffffffffu, ok);
 }
 
+// Copies one 128-value bf16 row (global, 16-byte aligned) into 64 TMEM columns
+// of this thread's lane, two values per column.  Zeros when `valid` is false.
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16* src, bool valid) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t r[32];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      uint4 x = valid ? __ldg(reinterpret_cast<const uint4*>(src) + half * 8 + v) : make_uint4(0, 0, 0, 0);
+      r[4 * v] = x.x;
+      r[4 * v + 1] = x.y;
+      r[4 * v + 2] = x.z;
+      r[4 * v + 3] = x.w;
+    }
+    ptx::tmem_st32(taddr + half * 32, r);
+  }
+}
+
+// Loads 64 fp32 columns of this lane (two x32 loads) and waits for them.
+__device__ __forceinline__ void ld64(uint32_t taddr, uint32_t (&r)[2][32]) {
+  ptx::tmem_ld32(taddr, r[0]);
+  ptx::tmem_ld32(taddr + 32, r[1]);
+  ptx::tmem_wait_ld_regs(r[0]);
+  ptx::tmem_wait_ld_regs(r[1]);
+}
+
 // ====================================================================== dK / dV
 
-constexpr int A_BK = 128;  // keys per CTA
-constexpr int A_BQ = 64;   // queries per tile
-constexpr int A_QST = 3;   // Q/dO stages
+constexpr int A_QST = 2;  // Q/dO stages
 
 struct ALayout {
-  static constexpr int kKV = A_BK * D * 2;       // 32 KB
-  static constexpr int kQT = A_BQ * D * 2;       // 16 KB
   static constexpr int kK = 0;
-  static constexpr int kV = kK + kKV;
-  static constexpr int kQ = kV + kKV;            // A_QST stages
-  static constexpr int kDO = kQ + A_QST * kQT;   // A_QST stages
-  static constexpr int kLse = kDO + A_QST * kQT;  // A_QST x (64 lse*log2e, 64 Delta)
-  static constexpr int kBar = kLse + A_QST * 2 * A_BQ * 4;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;            // A_QST stages
+  static constexpr int kDO = kQ + A_QST * kTileBytes;   // A_QST stages
+  static constexpr int kLse = kDO + A_QST * kTileBytes;  // A_QST x (128 lse, 128 Delta) fp32
+  static constexpr int kBar = kLse + A_QST * 2 * kTileRows * 4;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kSmemRequest = kBytes + 1024;
 };
@@ -101,9 +131,9 @@ struct ALayout {
 struct ABars {
   uint64_t kv_full;
   uint64_t q_full[A_QST], q_empty[A_QST];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t done;  // every MMA of the CTA has completed
+  uint64_t s_full, dp_full;  // S^T / dP^T of the current tile in TMEM
+  uint64_t p_full, ds_full;  // P^T / dS^T written back by the softmax
+  uint64_t done;             // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -141,19 +171,19 @@ __device__ __forceinline__ bool next_qtile(const Schedule& s, const KeyCtx& c, i
       i0 = 0;
       continue;
     }
-    const int nq = min(A_BQ, nq_seg - i0);
+    const int nq = min(kTileRows, nq_seg - i0);
     const int64_t pq_lo = (int64_t)poff + (int64_t)pst * i0;
     const int64_t pq_hi = pq_lo + (int64_t)pst * (nq - 1);
     const int icur = i0;
-    i0 += A_BQ;
+    i0 += kTileRows;
     if (c.causal && pq_hi < c.pk_lo) continue;  // every query before every key
     t.q_row = q_row0 + icur;
     t.nq = nq;
     t.pq_lo = pq_lo;
     t.qstride = pst;
     t.h = c.hk * c.G + hh;
-    t.full = (nq == A_BQ) && (c.causal ? pq_lo >= c.pk_hi : 1) && !c.docs;
-    if (c.docs && c.causal) t.full = (nq == A_BQ) && pq_lo >= c.pk_hi && c.en_lo > pq_hi;
+    t.full = (nq == kTileRows) && (c.causal ? pq_lo >= c.pk_hi : 1) && !c.docs;
+    if (c.docs && c.causal) t.full = (nq == kTileRows) && pq_lo >= c.pk_hi && c.en_lo > pq_hi;
     return true;
   }
   return false;
@@ -173,9 +203,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   float* lse_all = reinterpret_cast<float*>(smem + L::kLse);
 
   int g, tile, hk;
-  decode_unit(s, A_BK, a.Hkv, blockIdx.x, &g, &tile, &hk);
-  const int32_t k_row0 = s.g[g].q_row0 + tile * A_BK;  // key-major schedule: group = key run
-  const int nk_tile = min(A_BK, s.g[g].nq - tile * A_BK);
+  decode_unit(s, kTileRows, a.Hkv, blockIdx.x, &g, &tile, &hk);
+  const int32_t k_row0 = s.g[g].q_row0 + tile * kTileRows;  // key-major schedule: group = key run
+  const int nk_tile = min(kTileRows, s.g[g].nq - tile * kTileRows);
   const int seg_begin = s.g[g].seg_begin, seg_end = seg_begin + s.g[g].seg_count;
 
   KeyCtx c;
@@ -183,7 +213,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   c.docs = a.cu_seqlens != nullptr;
   c.G = a.Hq / a.Hkv;
   c.hk = hk;
-  c.pk_lo = (int64_t)s.g[g].pos_off + (int64_t)s.g[g].pos_stride * (tile * A_BK);
+  c.pk_lo = (int64_t)s.g[g].pos_off + (int64_t)s.g[g].pos_stride * (tile * kTileRows);
   c.pk_hi = c.pk_lo + (int64_t)s.g[g].pos_stride * (nk_tile - 1);
   c.en_lo = INT64_MAX;
   if (c.docs) {
@@ -194,13 +224,13 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < A_QST; ++i) {
-      ptx::mbar_init(&bars->q_full[i], 2);  // TMA (expect_tx) + the warp's lse/Delta stores
+      ptx::mbar_init(&bars->q_full[i], 1 + 32);  // TMA (expect_tx) + each producer lane's cp.async
       ptx::mbar_init(&bars->q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&bars->s_full[i], 1);
-      ptx::mbar_init(&bars->p_full[i], kWgThreads);
-    }
+    ptx::mbar_init(&bars->s_full, 1);
+    ptx::mbar_init(&bars->dp_full, 1);
+    ptx::mbar_init(&bars->p_full, kSoftmaxThreads);
+    ptx::mbar_init(&bars->ds_full, kSoftmaxThreads);
     ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -223,132 +253,128 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
 
   if (warp >= 8) {
     ptx::setmaxnreg_dec<kRegsLow>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer (whole warp)
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kKV);
-      for (int r = 0; r < D / 64; ++r) {
-        ptx::tma_load_2d(smem + L::kK + r * 16384, &tm_k, &bars->kv_full, hk * D + r * 64, k_row0);
-        ptx::tma_load_2d(smem + L::kV + r * 16384, &tm_v, &bars->kv_full, hk * D + r * 64, k_row0);
-      }
-    }
-    int hh = 0, seg = seg_begin, i0 = 0, j = 0;
-    QTile t;
-    int issued[A_QST] = {0, 0, 0};
-    while (__all_sync(0xffffffffu, *abort_flag == 0) &&
-           next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
-      const int st = j % A_QST;
-      if (j >= A_QST && !wait_all(&bars->q_empty[st], ((j / A_QST) - 1) & 1, abort_flag, a.err)) break;
+    if (warp == kProducerWarp) {
+      // ---------------------------------------------------------- producer (whole warp)
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&bars->q_full[st], 2 * L::kQT);
+        ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
         for (int r = 0; r < D / 64; ++r) {
-          ptx::tma_load_2d(smem + L::kQ + st * L::kQT + r * 8192, &tm_q, &bars->q_full[st],
-                           t.h * D + r * 64, t.q_row);
-          ptx::tma_load_2d(smem + L::kDO + st * L::kQT + r * 8192, &tm_do, &bars->q_full[st],
-                           t.h * D + r * 64, t.q_row);
+          ptx::tma_load_2d(smem + L::kK + r * 16384, &tm_k, &bars->kv_full, hk * D + r * 64, k_row0);
+          ptx::tma_load_2d(smem + L::kV + r * 16384, &tm_v, &bars->kv_full, hk * D + r * 64, k_row0);
         }
       }
-      float* lse_st = lse_all + st * 2 * A_BQ;
-      for (int cidx = lane; cidx < A_BQ; cidx += 32) {
-        float lv = INFINITY, dv = 0.f;  // +inf: rows past the run (or seeing nothing) get P = 0
-        if (cidx < t.nq) {
-          const float Lr = a.lse[(int64_t)t.h * a.lse_ld + t.q_row + cidx];
-          lv = (Lr == -INFINITY) ? INFINITY : Lr * kLog2e;
-          dv = a.delta[(int64_t)t.h * a.lse_ld + t.q_row + cidx];
+      int hh = 0, seg = seg_begin, i0 = 0, j = 0;
+      QTile t;
+      int issued[A_QST] = {0, 0};
+      while (__all_sync(0xffffffffu, *abort_flag == 0) &&
+             next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
+        const int st = j % A_QST;
+        if (j >= A_QST && !wait_all(&bars->q_empty[st], ((j / A_QST) - 1) & 1, abort_flag, a.err)) break;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&bars->q_full[st], 2 * kTileBytes);
+          for (int r = 0; r < D / 64; ++r) {
+            ptx::tma_load_2d(smem + L::kQ + st * kTileBytes + r * 16384, &tm_q, &bars->q_full[st],
+                             t.h * D + r * 64, t.q_row);
+            ptx::tma_load_2d(smem + L::kDO + st * kTileBytes + r * 16384, &tm_do, &bars->q_full[st],
+                             t.h * D + r * 64, t.q_row);
+          }
         }
-        lse_st[cidx] = lv;
-        lse_st[A_BQ + cidx] = dv;
+        // lse and Delta of the tile's rows (columns past the run are masked and never read)
+        float* lse_st = lse_all + st * 2 * kTileRows;
+        for (int cidx = lane; cidx < t.nq; cidx += 32) {
+          const int64_t off = (int64_t)t.h * a.lse_ld + t.q_row + cidx;
+          ptx::cp_async4(lse_st + cidx, a.lse + off);
+          ptx::cp_async4(lse_st + kTileRows + cidx, a.delta + off);
+        }
+        ptx::cp_async_arrive(&bars->q_full[st]);
+        issued[st] = j + 1;
+        ++j;
+      }
+      if (lane == 0 && *abort_flag) {
+        (void)ptx::mbar_wait_bounded(&bars->kv_full, 0, nullptr, nullptr, kDrainNs);
+        for (int st = 0; st < A_QST; ++st)
+          if (issued[st] > 0)
+            (void)ptx::mbar_wait_bounded(&bars->q_full[st], ((issued[st] - 1) / A_QST) & 1, nullptr,
+                                         nullptr, kDrainNs);
       }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->q_full[st]);
-      issued[st] = j + 1;
-      ++j;
-    }
-    if (lane == 0 && *abort_flag) {
-      (void)ptx::mbar_wait_bounded(&bars->kv_full, 0, nullptr, nullptr, kDrainNs);
-      for (int st = 0; st < A_QST; ++st)
-        if (issued[st] > 0)
-          (void)ptx::mbar_wait_bounded(&bars->q_full[st], ((issued[st] - 1) / A_QST) & 1, nullptr,
-                                       nullptr, kDrainNs);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, A_BQ, 0, 0);  // K Q^T, V dO^T
-      constexpr uint32_t id_kv = ptx::idesc_bf16_f32(128, D, 0, 1);    // P^T dO, dS^T Q (TMEM A)
-      const uint32_t k_addr = sbase + L::kK, v_addr = sbase + L::kV;
-      bool issued = false;
-      // S^T and dP^T of query tile jj into TMEM buffer jj & 1
-      auto issue_s = [&](int jj) -> bool {
-        const int st = jj % A_QST, b = jj & 1;
-        if (!ptx::mbar_wait_bounded(&bars->q_full[st], (jj / A_QST) & 1, abort_flag, a.err, kWaitNs))
-          return false;
-        ptx::tc_fence_after();
-        const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
-        const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16_ss(tmem + b * 128, desc_k(k_addr, kk, 16384), desc_k(q_addr, kk, 8192), id_s,
-                           kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          ptx::mma_bf16_ss(tmem + b * 128 + 64, desc_k(v_addr, kk, 16384), desc_k(do_addr, kk, 8192),
-                           id_s, kk > 0);
-        ptx::tc_commit(&bars->s_full[b]);
-        issued = true;
-        return true;
-      };
-      if (ptx::mbar_wait_bounded(&bars->kv_full, 0, abort_flag, a.err, kWaitNs)) {
-        int hh = 0, seg = seg_begin, i0 = 0;
-        QTile t;
-        int found = 0;  // query tiles the iterator has produced so far
-        bool exhausted = false;
-        auto advance = [&]() {
-          if (!exhausted) {
-            if (next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) ++found;
-            else exhausted = true;
-          }
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, 128, 0, 0);   // K Q^T, V dO^T
+        constexpr uint32_t id_kv = ptx::idesc_bf16_f32(128, D, 0, 1);    // P^T dO, dS^T Q (TMEM A)
+        const uint32_t k_addr = sbase + L::kK, v_addr = sbase + L::kV;
+        bool issued = false;
+        auto wait = [&](uint64_t* bar, uint32_t par) {
+          return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
         };
-        bool fail = false;
-        advance();
-        if (found > 0 && !issue_s(0)) fail = true;
-        advance();
-        if (!fail && found > 1 && !issue_s(1)) fail = true;
-        for (int j = 0; !fail && j < found; ++j) {
-          const int b = j & 1, st = j % A_QST;
-          if (!ptx::mbar_wait_bounded(&bars->p_full[b], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
-          ptx::tc_fence_after();
-          const uint32_t q_addr = sbase + L::kQ + st * L::kQT;
-          const uint32_t do_addr = sbase + L::kDO + st * L::kQT;
-          // P^T / dS^T: 64 queries packed two per column (K step kk = 8 columns)
+        auto scores = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr) {
 #pragma unroll
-          for (int kk = 0; kk < A_BQ / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + 256, tmem + b * 128 + kk * 8, desc_mn(do_addr, kk, 8192), id_kv,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16_ss(tmem + d, desc_k(a_addr, kk), desc_k(b_addr, kk), id_s, kk > 0);
+        };
+        auto grads = [&](uint32_t d, uint32_t a_tmem, uint32_t b_addr, bool acc) {
 #pragma unroll
-          for (int kk = 0; kk < A_BQ / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + 384, tmem + b * 128 + 64 + kk * 8, desc_mn(q_addr, kk, 8192), id_kv,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::tc_commit(&bars->q_empty[st]);
-          advance();
-          if (found > j + 2 && !issue_s(j + 2)) break;  // reuses buffer b after these products
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            ptx::mma_bf16_ts(tmem + d, a_split(tmem + a_tmem, kk), desc_mn(b_addr, kk), id_kv,
+                             (acc || kk > 0) ? 1u : 0u);
+        };
+        if (wait(&bars->kv_full, 0)) {
+          int hh = 0, seg = seg_begin, i0 = 0, j = 0;
+          QTile t;
+          bool have = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+          if (have) {
+            if (!wait(&bars->q_full[0], 0)) have = false;
+            if (have) {
+              ptx::tc_fence_after();
+              scores(0, k_addr, sbase + L::kQ);
+              ptx::tc_commit(&bars->s_full);
+              scores(128, v_addr, sbase + L::kDO);
+              ptx::tc_commit(&bars->dp_full);
+              issued = true;
+            }
+          }
+          while (have) {
+            const bool more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+            const int st = j % A_QST, st1 = (j + 1) % A_QST;
+            // dV += P^T dO once P^T is written back
+            if (!wait(&bars->p_full, j & 1)) break;
+            ptx::tc_fence_after();
+            grads(256, 0, sbase + L::kDO + st * kTileBytes, j > 0);
+            // next tile's S^T (reuses the S^T columns after dV has read P^T)
+            if (more) {
+              if (!wait(&bars->q_full[st1], ((j + 1) / A_QST) & 1)) break;
+              ptx::tc_fence_after();
+              scores(0, k_addr, sbase + L::kQ + st1 * kTileBytes);
+              ptx::tc_commit(&bars->s_full);
+            }
+            // dK += dS^T Q once dS^T is written back
+            if (!wait(&bars->ds_full, j & 1)) break;
+            ptx::tc_fence_after();
+            grads(384, 128, sbase + L::kQ + st * kTileBytes, j > 0);
+            ptx::tc_commit(&bars->q_empty[st]);
+            if (more) {
+              scores(128, v_addr, sbase + L::kDO + st1 * kTileBytes);
+              ptx::tc_commit(&bars->dp_full);
+            }
+            ++j;
+            have = more;
+          }
+        }
+        if (issued) {
+          ptx::tc_commit(&bars->done);
+          (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
+        } else {
+          ptx::mbar_arrive(&bars->done);
         }
       }
-      if (issued) {
-        ptx::tc_commit(&bars->done);
-        (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
-      } else {
-        ptx::mbar_arrive(&bars->done);
-      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     ptx::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax warpgroups (thread = key row)
     const int quad = warp & 3;
-    const int w = warp >> 2;  // this warpgroup takes the query tiles j with j % 2 == w
+    const int wg = warp >> 2;
+    const int cb = wg * 64;  // this warpgroup's 64 query columns of the 128
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const int64_t pk = c.pk_lo + (int64_t)s.g[g].pos_stride * r;
@@ -360,11 +386,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     bool ok = true;
     while (__all_sync(0xffffffffu, *abort_flag == 0) &&
            next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
-      if ((j & 1) != w) {
-        ++j;
-        continue;
-      }
-      const int st = j % A_QST, b = w;
+      const int st = j % A_QST;
       int64_t hi = t.nq - 1, lo = 0;  // visible query columns of this key row: [lo, hi]
       if (r >= nk_tile) {
         hi = -1;
@@ -383,47 +405,63 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         }
       }
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
-      // lse/Delta of this tile were stored by the producer before q_full completed
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
-      if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+      const float* lse_st = lse_all + st * 2 * kTileRows + cb;
+      const float* del_st = lse_st + kTileRows;
+      // phase 1: P^T = 2^(S^T*scale*log2e - lse*log2e)
+      if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
-      ptx::tmem_wait_ld_regs(sr[0]);
-      ptx::tmem_wait_ld_regs(sr[1]);
-      ptx::tmem_wait_ld_regs(dr[0]);
-      ptx::tmem_wait_ld_regs(dr[1]);
-      const float* lse_st = lse_all + st * 2 * A_BQ;
-      uint32_t pp[32], dd[32];
+      float p[64];
+      {
+        uint32_t sr[2][32];
+        ld64(lane_addr + cb, sr);
 #pragma unroll
-      for (int cc = 0; cc < A_BQ; cc += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cc);
-        const float4 d4 = *reinterpret_cast<const float4*>(lse_st + A_BQ + cc);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-        float p[4], ds[4];
+        for (int cc = 0; cc < 64; cc += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cc);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int col = cc + u;
-          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
-          p[u] = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lv[u])) : 0.f;
-          ds[u] = p[u] * (dp - dl[u]);
+          for (int u = 0; u < 4; ++u) {
+            const int col = cc + u;
+            const bool vis = cb + col >= ilo && cb + col <= ihi;  // masked columns read nothing staged
+            const float sv = __uint_as_float(sr[col >> 5][col & 31]);
+            p[col] = vis ? ptx::ex2_approx(fmaf(sv, sl2, -lv[u] * kLog2e)) : 0.f;
+          }
         }
-        pp[cc / 2] = ptx::pack_bf16x2(p[0], p[1]);
-        pp[cc / 2 + 1] = ptx::pack_bf16x2(p[2], p[3]);
-        dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
-        dd[cc / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+        uint32_t pk32[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk32[i] = ptx::pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        ptx::tmem_st32(lane_addr + cb, pk32);  // P^T over the first 32 of this warpgroup's columns
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->p_full);
       }
-      // P^T and dS^T (two bf16 per column) over the S^T / dP^T columns just read
-      ptx::tmem_st32(lane_addr + b * 128, pp);
-      ptx::tmem_st32(lane_addr + b * 128 + 64, dd);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->p_full[b]);
+      // phase 2: dS^T = P^T o (dP^T - Delta)
+      if (!wait_all(&bars->dp_full, j & 1, abort_flag, a.err)) { ok = false; break; }
+      ptx::tc_fence_after();
+      {
+        uint32_t dr[2][32];
+        ld64(lane_addr + 128 + cb, dr);
+        uint32_t dd[32];
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(del_st + cc);
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = cc + u;
+            const bool vis = cb + col >= ilo && cb + col <= ihi;
+            const float dp = __uint_as_float(dr[col >> 5][col & 31]);
+            ds[u] = vis ? p[col] * (dp - dl[u]) : 0.f;
+          }
+          dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
+          dd[cc / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+        }
+        ptx::tmem_st32(lane_addr + 128 + cb, dd);  // dS^T over the first 32 of this warpgroup's dP^T columns
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->ds_full);
+      }
       ++j;
     }
     // ------------------------------------------------------------ dK / dV epilogue
@@ -433,28 +471,25 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       ptx::tc_fence_after();
       const bool valid = r < nk_tile;
       const int64_t krow = (int64_t)(k_row0 + r) * a.k_ld + (int64_t)hk * D;
-      {
-        const int which = warp >> 2;  // warpgroup 0 stores dV, warpgroup 1 stores dK
-        float* dst = (which == 0 ? a.dv_acc : a.dk_acc) + krow;
-        const float mul = which == 0 ? 1.f : a.scale;
-        const uint32_t col0 = which == 0 ? 256 : 384;
+      float* dst = (wg == 0 ? a.dv_acc : a.dk_acc) + krow;  // warpgroup 0: dV, 1: dK
+      const float mul = wg == 0 ? 1.f : a.scale;
+      const uint32_t col0 = wg == 0 ? 256 : 384;
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t rr[32];
-          if (j > 0) {
-            ptx::tmem_ld32(lane_addr + col0 + ch * 32, rr);
-            ptx::tmem_wait_ld_regs(rr);
-          } else {
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t rr[32];
+        if (j > 0) {
+          ptx::tmem_ld32(lane_addr + col0 + ch * 32, rr);
+          ptx::tmem_wait_ld_regs(rr);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = 0u;
-          }
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
+        if (valid) {
+          float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              d4[v4] = make_float4(__uint_as_float(rr[4 * v4]) * mul, __uint_as_float(rr[4 * v4 + 1]) * mul,
-                                   __uint_as_float(rr[4 * v4 + 2]) * mul, __uint_as_float(rr[4 * v4 + 3]) * mul);
-          }
+          for (int v4 = 0; v4 < 8; ++v4)
+            d4[v4] = make_float4(__uint_as_float(rr[4 * v4]) * mul, __uint_as_float(rr[4 * v4 + 1]) * mul,
+                                 __uint_as_float(rr[4 * v4 + 2]) * mul, __uint_as_float(rr[4 * v4 + 3]) * mul);
         }
       }
     }
@@ -470,28 +505,23 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
 
 // ====================================================================== dQ
 
-constexpr int B_BQ = 128;  // query rows per CTA
-constexpr int B_BN = 64;   // keys per tile
-constexpr int B_KST = 3;   // K/V stages
+constexpr int B_KST = 3;  // K/V stages
 
 struct BLayout {
-  static constexpr int kQT = B_BQ * D * 2;   // 32 KB
-  static constexpr int kKT = B_BN * D * 2;   // 16 KB
-  static constexpr int kQ = 0;
-  static constexpr int kDO = kQ + kQT;
-  static constexpr int kK = kDO + kQT;       // B_KST stages
-  static constexpr int kV = kK + B_KST * kKT;
-  static constexpr int kBar = kV + B_KST * kKT;
+  static constexpr int kK = 0;                          // B_KST stages
+  static constexpr int kV = kK + B_KST * kTileBytes;
+  static constexpr int kBar = kV + B_KST * kTileBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kSmemRequest = kBytes + 1024;
 };
 
 struct BBars {
-  uint64_t q_full;
+  uint64_t q_full;  // Q and dO copied into TMEM
   uint64_t k_full[B_KST], v_full[B_KST], kv_empty[B_KST];
-  uint64_t s_full[2];
-  uint64_t ds_full[2];
-  uint64_t done;  // every MMA of the CTA has completed
+  uint64_t s_full, dp_full;  // S / dP of the current tile in TMEM
+  uint64_t s_free;           // the softmax has read S
+  uint64_t ds_full;          // dS written back
+  uint64_t done;             // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -510,7 +540,7 @@ struct KvTile {
   int32_t full;
 };
 
-// Next key/value tile (64 keys) of the query group with any visible pair.
+// Next key/value tile (128 keys) of the query group with any visible pair.
 __device__ __forceinline__ bool next_ktile(const Schedule& s, const TileCtx& c, int seg_end, int& seg,
                                            int& j0, KvTile& t) {
   while (seg < seg_end) {
@@ -521,11 +551,11 @@ __device__ __forceinline__ bool next_ktile(const Schedule& s, const TileCtx& c, 
       j0 = 0;
       continue;
     }
-    const int nk = min(B_BN, nk_seg - j0);
+    const int nk = min(kTileRows, nk_seg - j0);
     const int64_t pk_lo = (int64_t)poff + (int64_t)pst * j0;
     const int64_t pk_hi = pk_lo + (int64_t)pst * (nk - 1);
     const int jcur = j0;
-    j0 += B_BN;
+    j0 += kTileRows;
     if ((c.causal && pk_lo > c.pq_hi) || (c.docs && pk_lo >= c.en_hi)) {
       ++seg;
       j0 = 0;
@@ -536,7 +566,7 @@ __device__ __forceinline__ bool next_ktile(const Schedule& s, const TileCtx& c, 
     t.nk = nk;
     t.pk_lo = pk_lo;
     t.kstride = pst;
-    t.full = (nk == B_BN) && (!c.causal || pk_hi <= c.pq_lo) &&
+    t.full = (nk == kTileRows) && (!c.causal || pk_hi <= c.pq_lo) &&
              (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo));
     return true;
   }
@@ -545,7 +575,6 @@ __device__ __forceinline__ bool next_ktile(const Schedule& s, const TileCtx& c, 
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Schedule s,
-                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = BLayout;
   extern __shared__ uint8_t smem_raw[];
@@ -556,13 +585,13 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int g, tile, h;
-  decode_unit(s, B_BQ, a.Hq, blockIdx.x, &g, &tile, &h);
+  decode_unit(s, kTileRows, a.Hq, blockIdx.x, &g, &tile, &h);
   const int hk = h / (a.Hq / a.Hkv);
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
   const int32_t qpos_off = s.g[g].pos_off, qpos_st = s.g[g].pos_stride;
   const int seg_begin = s.g[g].seg_begin, seg_end = seg_begin + s.g[g].seg_count;
-  const int i0 = tile * B_BQ;
-  const int nq_tile = min(B_BQ, nq - i0);
+  const int i0 = tile * kTileRows;
+  const int nq_tile = min(kTileRows, nq - i0);
 
   TileCtx c;
   c.causal = a.causal;
@@ -576,16 +605,16 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   }
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, 1);
+    ptx::mbar_init(&bars->q_full, kSoftmaxThreads);
     for (int i = 0; i < B_KST; ++i) {
       ptx::mbar_init(&bars->k_full[i], 1);
       ptx::mbar_init(&bars->v_full[i], 1);
       ptx::mbar_init(&bars->kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&bars->s_full[i], 1);
-      ptx::mbar_init(&bars->ds_full[i], kWgThreads);
-    }
+    ptx::mbar_init(&bars->s_full, 1);
+    ptx::mbar_init(&bars->dp_full, 1);
+    ptx::mbar_init(&bars->s_free, kSoftmaxThreads);
+    ptx::mbar_init(&bars->ds_full, kSoftmaxThreads);
     ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -595,8 +624,6 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     ptx::tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) {
-    ptx::prefetch_tensormap(&tm_q);
-    ptx::prefetch_tensormap(&tm_do);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
   }
@@ -608,119 +635,135 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
 
   if (warp >= 8) {
     ptx::setmaxnreg_dec<kRegsLow>();
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * L::kQT);
-      for (int r = 0; r < D / 64; ++r) {
-        ptx::tma_load_2d(smem + L::kQ + r * 16384, &tm_q, &bars->q_full, h * D + r * 64, q_row0 + i0);
-        ptx::tma_load_2d(smem + L::kDO + r * 16384, &tm_do, &bars->q_full, h * D + r * 64, q_row0 + i0);
-      }
-      int seg = seg_begin, j0 = 0, j = 0;
-      KvTile t;
-      int issued[B_KST] = {0, 0, 0};
-      while (!*abort_flag && next_ktile(s, c, seg_end, seg, j0, t)) {
-        const int st = j % B_KST;
-        if (j >= B_KST && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j / B_KST) - 1) & 1, abort_flag,
-                                                   a.err, kWaitNs))
-          break;
-        ptx::mbar_arrive_expect_tx(&bars->k_full[st], L::kKT);
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_2d(smem + L::kK + st * L::kKT + r * 8192, &tm_k, &bars->k_full[st],
-                           hk * D + r * 64, t.k_row);
-        ptx::mbar_arrive_expect_tx(&bars->v_full[st], L::kKT);
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_2d(smem + L::kV + st * L::kKT + r * 8192, &tm_v, &bars->v_full[st],
-                           hk * D + r * 64, t.k_row);
-        issued[st] = j + 1;
-        ++j;
-      }
-      if (*abort_flag) {
-        (void)ptx::mbar_wait_bounded(&bars->q_full, 0, nullptr, nullptr, kDrainNs);
-        for (int st = 0; st < B_KST; ++st)
-          if (issued[st] > 0) {
-            const uint32_t par = ((issued[st] - 1) / B_KST) & 1;
-            (void)ptx::mbar_wait_bounded(&bars->k_full[st], par, nullptr, nullptr, kDrainNs);
-            (void)ptx::mbar_wait_bounded(&bars->v_full[st], par, nullptr, nullptr, kDrainNs);
-          }
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = ptx::idesc_bf16_f32(B_BQ, B_BN, 0, 0);  // Q K^T, dO V^T
-      constexpr uint32_t id_q = ptx::idesc_bf16_f32(B_BQ, D, 0, 1);     // dS K
-      const uint32_t q_addr = sbase + L::kQ, do_addr = sbase + L::kDO;
-      bool any = false;
-      if (ptx::mbar_wait_bounded(&bars->q_full, 0, abort_flag, a.err, kWaitNs)) {
+    if (warp == kProducerWarp) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
         int seg = seg_begin, j0 = 0, j = 0;
         KvTile t;
-        bool more = next_ktile(s, c, seg_end, seg, j0, t);
-        while (true) {
-          if (more) {
-            const int st = j % B_KST, b = j & 1;
-            if (!ptx::mbar_wait_bounded(&bars->k_full[st], (j / B_KST) & 1, abort_flag, a.err, kWaitNs))
-              break;
-            if (!ptx::mbar_wait_bounded(&bars->v_full[st], (j / B_KST) & 1, abort_flag, a.err, kWaitNs))
-              break;
-            ptx::tc_fence_after();
-            const uint32_t k_addr = sbase + L::kK + st * L::kKT;
-            const uint32_t v_addr = sbase + L::kV + st * L::kKT;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + b * 128, desc_k(q_addr, kk, 16384), desc_k(k_addr, kk, 8192), id_s,
-                               kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              ptx::mma_bf16_ss(tmem + b * 128 + 64, desc_k(do_addr, kk, 16384), desc_k(v_addr, kk, 8192),
-                               id_s, kk > 0);
-            ptx::tc_commit(&bars->s_full[b]);
-            any = true;
-          }
-          if (j >= 1) {
-            const int jp = j - 1, stp = jp % B_KST, bp = jp & 1;
-            if (!ptx::mbar_wait_bounded(&bars->ds_full[bp], (jp >> 1) & 1, abort_flag, a.err, kWaitNs))
-              break;
-            ptx::tc_fence_after();
-            const uint32_t k_addr = sbase + L::kK + stp * L::kKT;
-            // dS: 64 keys packed two per column over the dP columns (K step kk = 8 columns)
-#pragma unroll
-            for (int kk = 0; kk < B_BN / 16; ++kk)
-              ptx::mma_bf16_ts(tmem + 256, tmem + bp * 128 + 64 + kk * 8, desc_mn(k_addr, kk, 8192), id_q,
-                               (jp > 0 || kk > 0) ? 1u : 0u);
-            ptx::tc_commit(&bars->kv_empty[stp]);
-          }
-          if (!more) break;
+        int issued[B_KST] = {0, 0, 0};
+        while (!*abort_flag && next_ktile(s, c, seg_end, seg, j0, t)) {
+          const int st = j % B_KST;
+          if (j >= B_KST && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j / B_KST) - 1) & 1, abort_flag,
+                                                     a.err, kWaitNs))
+            break;
+          ptx::mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+          for (int r = 0; r < D / 64; ++r)
+            ptx::tma_load_2d(smem + L::kK + st * kTileBytes + r * 16384, &tm_k, &bars->k_full[st],
+                             hk * D + r * 64, t.k_row);
+          ptx::mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+          for (int r = 0; r < D / 64; ++r)
+            ptx::tma_load_2d(smem + L::kV + st * kTileBytes + r * 16384, &tm_v, &bars->v_full[st],
+                             hk * D + r * 64, t.k_row);
+          issued[st] = j + 1;
           ++j;
-          more = next_ktile(s, c, seg_end, seg, j0, t);
+        }
+        if (*abort_flag) {
+          for (int st = 0; st < B_KST; ++st)
+            if (issued[st] > 0) {
+              const uint32_t par = ((issued[st] - 1) / B_KST) & 1;
+              (void)ptx::mbar_wait_bounded(&bars->k_full[st], par, nullptr, nullptr, kDrainNs);
+              (void)ptx::mbar_wait_bounded(&bars->v_full[st], par, nullptr, nullptr, kDrainNs);
+            }
         }
       }
-      if (any) {
-        ptx::tc_commit(&bars->done);
-        (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
-      } else {
-        ptx::mbar_arrive(&bars->done);
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K^T, dO V^T (TMEM A)
+        constexpr uint32_t id_q = ptx::idesc_bf16_f32(128, D, 0, 1);    // dS K (TMEM A)
+        bool any = false;
+        auto wait = [&](uint64_t* bar, uint32_t par) {
+          return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
+        };
+        auto scores = [&](uint32_t d, uint32_t a_tmem, uint32_t b_addr) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            ptx::mma_bf16_ts(tmem + d, tmem + a_tmem + kk * 8, desc_k(b_addr, kk), id_s, kk > 0);
+        };
+        if (wait(&bars->q_full, 0)) {
+          ptx::tc_fence_after();
+          int seg = seg_begin, j0 = 0, j = 0;
+          KvTile t;
+          bool have = next_ktile(s, c, seg_end, seg, j0, t);
+          if (have) {
+            have = wait(&bars->k_full[0], 0) && wait(&bars->v_full[0], 0);
+            if (have) {
+              ptx::tc_fence_after();
+              scores(0, 384, sbase + L::kK);
+              ptx::tc_commit(&bars->s_full);
+              scores(128, 448, sbase + L::kV);
+              ptx::tc_commit(&bars->dp_full);
+              any = true;
+            }
+          }
+          while (have) {
+            const bool more = next_ktile(s, c, seg_end, seg, j0, t);
+            const int st = j % B_KST, st1 = (j + 1) % B_KST, par1 = ((j + 1) / B_KST) & 1;
+            // next tile's S once the softmax has read this tile's S
+            if (more) {
+              if (!wait(&bars->s_free, j & 1)) break;
+              if (!wait(&bars->k_full[st1], par1)) break;
+              ptx::tc_fence_after();
+              scores(0, 384, sbase + L::kK + st1 * kTileBytes);
+              ptx::tc_commit(&bars->s_full);
+            }
+            // dQ += dS K once dS is written back (dS: two warpgroup halves of 64 keys)
+            if (!wait(&bars->ds_full, j & 1)) break;
+            ptx::tc_fence_after();
+            {
+              const uint32_t k_addr = sbase + L::kK + st * kTileBytes;
+#pragma unroll
+              for (int kk = 0; kk < kTileRows / 16; ++kk)
+                ptx::mma_bf16_ts(tmem + 256, a_split(tmem + 128, kk), desc_mn(k_addr, kk), id_q,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::tc_commit(&bars->kv_empty[st]);
+            // next tile's dP (reuses the dP columns after dQ has read dS)
+            if (more) {
+              if (!wait(&bars->v_full[st1], par1)) break;
+              ptx::tc_fence_after();
+              scores(128, 448, sbase + L::kV + st1 * kTileBytes);
+              ptx::tc_commit(&bars->dp_full);
+            }
+            ++j;
+            have = more;
+          }
+        }
+        if (any) {
+          ptx::tc_commit(&bars->done);
+          (void)ptx::mbar_wait_bounded(&bars->done, 0, nullptr, a.err, kWaitNs);
+        } else {
+          ptx::mbar_arrive(&bars->done);
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     ptx::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax warpgroups (thread = query row)
     const int quad = warp & 3;
-    const int w = warp >> 2;  // this warpgroup takes the key tiles j with j % 2 == w
+    const int w = warp >> 2;
+    const int cb = w * 64;  // this warpgroup's 64 key columns of the 128
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-    const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
     const bool row_valid = r < nq_tile;
+    // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, once
+    {
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(w == 0 ? a.q : a.dout) +
+                                 (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
+      row_to_tmem(lane_addr + 384 + w * 64, src, row_valid);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->q_full);
+    }
+    const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
     int64_t st_r = 0, en_r = 0;
     if (c.docs && row_valid) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
-    float lse2 = INFINITY, delta = 0.f;
+    float nlse2 = 0.f, delta = 0.f;  // -lse*log2(e); rows without a visible key are fully masked
     if (row_valid) {
       const int64_t col = (int64_t)h * a.lse_ld + q_row0 + i0 + r;
-      const float Lr = a.lse[col];
-      lse2 = (Lr == -INFINITY) ? INFINITY : Lr * kLog2e;
+      nlse2 = -a.lse[col] * kLog2e;
       delta = a.delta[col];
     }
     const float sl2 = a.scale_log2;
@@ -728,13 +771,10 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     KvTile t;
     bool ok = true;
     while (__all_sync(0xffffffffu, *abort_flag == 0) && next_ktile(s, c, seg_end, seg, j0, t)) {
-      if ((j & 1) != w) {
-        ++j;
-        continue;
-      }
-      const int b = w;
       int64_t hi = t.nk - 1, lo = 0;
-      if (!t.full) {
+      if (!row_valid) {
+        hi = -1;
+      } else if (!t.full) {
         if (c.causal) {
           const int64_t d = pq - t.pk_lo;
           hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
@@ -747,36 +787,41 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         }
       }
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
-      if (!wait_all(&bars->s_full[b], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+      // phase 1: P from S, then release S for the next tile
+      if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      ptx::tmem_ld32(lane_addr + b * 128 + 0, sr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 32, sr[1]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 64, dr[0]);
-      ptx::tmem_ld32(lane_addr + b * 128 + 96, dr[1]);
-      ptx::tmem_wait_ld_regs(sr[0]);
-      ptx::tmem_wait_ld_regs(sr[1]);
-      ptx::tmem_wait_ld_regs(dr[0]);
-      ptx::tmem_wait_ld_regs(dr[1]);
-      uint32_t dd[32];
+      float p[64];
+      {
+        uint32_t sr[2][32];
+        ld64(lane_addr + cb, sr);
 #pragma unroll
-      for (int cc = 0; cc < B_BN; cc += 2) {
-        float ds[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = cc + u;
-          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-          const float dp = __uint_as_float(dr[col >> 5][col & 31]);
-          const float p = (col >= ilo && col <= ihi) ? ptx::ex2_approx(fmaf(sv, sl2, -lse2)) : 0.f;
-          ds[u] = p * (dp - delta);
+        for (int col = 0; col < 64; ++col) {
+          const bool vis = cb + col >= ilo && cb + col <= ihi;
+          p[col] = vis ? ptx::ex2_approx(fmaf(__uint_as_float(sr[col >> 5][col & 31]), sl2, nlse2)) : 0.f;
         }
-        dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
       }
-      // dS (two bf16 per column) over the dP columns just read
-      ptx::tmem_st32(lane_addr + b * 128 + 64, dd);
-      ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->ds_full[b]);
+      ptx::mbar_arrive(&bars->s_free);
+      // phase 2: dS = P o (dP - Delta), written over dP
+      if (!wait_all(&bars->dp_full, j & 1, abort_flag, a.err)) { ok = false; break; }
+      ptx::tc_fence_after();
+      {
+        uint32_t dr[2][32];
+        ld64(lane_addr + 128 + cb, dr);
+        uint32_t dd[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c0 = 2 * i, c1 = 2 * i + 1;
+          const bool v0 = cb + c0 >= ilo && cb + c0 <= ihi, v1 = cb + c1 >= ilo && cb + c1 <= ihi;
+          const float ds0 = v0 ? p[c0] * (__uint_as_float(dr[c0 >> 5][c0 & 31]) - delta) : 0.f;
+          const float ds1 = v1 ? p[c1] * (__uint_as_float(dr[c1 >> 5][c1 & 31]) - delta) : 0.f;
+          dd[i] = ptx::pack_bf16x2(ds0, ds1);
+        }
+        ptx::tmem_st32(lane_addr + 128 + cb, dd);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->ds_full);
+      }
       ++j;
     }
     // ------------------------------------------------------------ dQ epilogue
@@ -786,7 +831,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       ptx::tc_fence_after();
       float* dst = a.dq_acc + (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
 #pragma unroll
-      for (int ch = (warp >> 2) * 2; ch < (warp >> 2) * 2 + 2; ++ch) {  // 64 columns per warpgroup
+      for (int ch = w * 2; ch < w * 2 + 2; ++ch) {  // 64 columns per warpgroup
         uint32_t rr[32];
         if (j > 0) {
           ptx::tmem_ld32(lane_addr + 256 + ch * 32, rr);
@@ -836,7 +881,8 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+// 2-D map over a [rows, H*D] bf16 buffer; box 64 columns x 128 rows, 128-byte swizzle.
+cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) {
     set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
@@ -844,7 +890,7 @@ cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
   }
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileRows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -914,17 +960,6 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
     set_last_error("tcgen05 attention backward supports D = 128");
     return CP_ERR_UNSUPPORTED;
   }
-  CUtensorMap mq64, mdo64, mk128, mv128, mq128, mdo128, mk64, mv64;
-  cp_status r;
-  if ((r = make_map(&mq64, a.q, q_rows, (int64_t)a.Hq * D, A_BQ)) != CP_OK) return r;
-  if ((r = make_map(&mdo64, a.dout, q_rows, (int64_t)a.Hq * D, A_BQ)) != CP_OK) return r;
-  if ((r = make_map(&mk128, a.k, k_rows, (int64_t)a.Hkv * D, A_BK)) != CP_OK) return r;
-  if ((r = make_map(&mv128, a.v, k_rows, (int64_t)a.Hkv * D, A_BK)) != CP_OK) return r;
-  if ((r = make_map(&mq128, a.q, q_rows, (int64_t)a.Hq * D, B_BQ)) != CP_OK) return r;
-  if ((r = make_map(&mdo128, a.dout, q_rows, (int64_t)a.Hq * D, B_BQ)) != CP_OK) return r;
-  if ((r = make_map(&mk64, a.k, k_rows, (int64_t)a.Hkv * D, B_BN)) != CP_OK) return r;
-  if ((r = make_map(&mv64, a.v, k_rows, (int64_t)a.Hkv * D, B_BN)) != CP_OK) return r;
-
   // setmaxnreg.inc waits until the registers it asks for are free in the block's launch
   // budget, so launch only if each kernel's compiled register count covers the split.
   for (const void* kfn : {(const void*)attn_bwd_dkdv_kernel, (const void*)attn_bwd_dq_kernel}) {
@@ -937,14 +972,20 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
       return CP_ERR_UNSUPPORTED;
     }
   }
+  CUtensorMap mq, mdo, mk, mv;
+  cp_status r;
+  if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * D)) != CP_OK) return r;
+  if ((r = make_map(&mdo, a.dout, q_rows, (int64_t)a.Hq * D)) != CP_OK) return r;
+  if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * D)) != CP_OK) return r;
+  if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * D)) != CP_OK) return r;
+
   // dK / dV over the key-major schedule
-  int64_t units = schedule_units(s, A_BK, a.Hkv);
+  int64_t units = schedule_units(s, kTileRows, a.Hkv);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          ALayout::kSmemRequest);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dkdv)");
-    attn_bwd_dkdv_kernel<<<(unsigned)units, kThreads, ALayout::kSmemRequest, st>>>(a, s, mq64, mdo64,
-                                                                                    mk128, mv128);
+    attn_bwd_dkdv_kernel<<<(unsigned)units, kThreads, ALayout::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
     if ((r = cuda_check(cudaGetLastError(), "attn_bwd_dkdv_kernel launch")) != CP_OK) return r;
   }
   // dQ over the query-major schedule (same pairs)
@@ -954,7 +995,7 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
     set_last_error("backward schedule too large to invert");
     return CP_ERR_UNSUPPORTED;
   }
-  units = schedule_units(*qm, B_BQ, a.Hq);
+  units = schedule_units(*qm, kTileRows, a.Hq);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          BLayout::kSmemRequest);
@@ -962,8 +1003,7 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
       delete qm;
       return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dq)");
     }
-    attn_bwd_dq_kernel<<<(unsigned)units, kThreads, BLayout::kSmemRequest, st>>>(a, *qm, mq128, mdo128,
-                                                                                  mk64, mv64);
+    attn_bwd_dq_kernel<<<(unsigned)units, kThreads, BLayout::kSmemRequest, st>>>(a, *qm, mk, mv);
     r = cuda_check(cudaGetLastError(), "attn_bwd_dq_kernel launch");
   }
   delete qm;
