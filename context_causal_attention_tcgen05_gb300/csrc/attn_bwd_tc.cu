@@ -105,14 +105,6 @@ __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16*
   }
 }
 
-// Loads 64 fp32 columns of this lane (two x32 loads) and waits for them.
-__device__ __forceinline__ void ld64(uint32_t taddr, uint32_t (&r)[2][32]) {
-  ptx::tmem_ld32(taddr, r[0]);
-  ptx::tmem_ld32(taddr + 32, r[1]);
-  ptx::tmem_wait_ld_regs(r[0]);
-  ptx::tmem_wait_ld_regs(r[1]);
-}
-
 // ====================================================================== dK / dV
 
 constexpr int A_QST = 2;  // Q/dO stages
@@ -381,6 +373,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     int64_t st_k = 0, en_k = INT64_MAX;
     if (c.docs && r < nk_tile) doc_bounds(a.cu_seqlens, a.n_docs, pk, &st_k, &en_k);
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nlog2e2 = ptx::f2_pack(-kLog2e, -kLog2e);
+    const uint64_t neg1x2 = ptx::f2_pack(-1.f, -1.f);
     int hh = 0, seg = seg_begin, i0 = 0, j = 0;
     QTile t;
     bool ok = true;
@@ -408,25 +402,42 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
       const float* lse_st = lse_all + st * 2 * kTileRows + cb;
       const float* del_st = lse_st + kTileRows;
-      // phase 1: P^T = 2^(S^T*scale*log2e - lse*log2e)
+      // phase 1: P^T = 2^(S^T*scale*log2e - lse*log2e), 32 columns at a time
       if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
       float p[64];
-      {
-        uint32_t sr[2][32];
-        ld64(lane_addr + cb, sr);
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_st + cc);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      for (int hc = 0; hc < 64; hc += 32) {
+        uint32_t sr[32];
+        ptx::tmem_ld32(lane_addr + cb + hc, sr);
+        ptx::tmem_wait_ld_regs(sr);
+        if (t.full) {  // every pair visible: no per-column mask
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int col = cc + u;
-            const bool vis = cb + col >= ilo && cb + col <= ihi;  // masked columns read nothing staged
-            const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-            p[col] = vis ? ptx::ex2_approx(fmaf(sv, sl2, -lv[u] * kLog2e)) : 0.f;
+          for (int cc = 0; cc < 32; cc += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_st + hc + cc);
+            const uint64_t nl01 = ptx::fmul2(ptx::f2_pack(l4.x, l4.y), nlog2e2);
+            const uint64_t nl23 = ptx::fmul2(ptx::f2_pack(l4.z, l4.w), nlog2e2);
+            float a0, a1, a2, a3;
+            ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])),
+                                      sl2x2, nl01), a0, a1);
+            ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3])),
+                                      sl2x2, nl23), a2, a3);
+            p[hc + cc] = ptx::ex2_approx(a0);
+            p[hc + cc + 1] = ptx::ex2_approx(a1);
+            p[hc + cc + 2] = ptx::ex2_approx(a2);
+            p[hc + cc + 3] = ptx::ex2_approx(a3);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const int col = cb + hc + cc;
+            const bool vis = col >= ilo && col <= ihi;  // masked columns read nothing staged
+            p[hc + cc] = vis ? ptx::ex2_approx(fmaf(__uint_as_float(sr[cc]), sl2, -lse_st[hc + cc] * kLog2e))
+                             : 0.f;
           }
         }
+      }
+      {
         uint32_t pk32[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk32[i] = ptx::pack_bf16x2(p[2 * i], p[2 * i + 1]);
@@ -435,33 +446,42 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bars->p_full);
       }
-      // phase 2: dS^T = P^T o (dP^T - Delta)
+      // phase 2: dS^T = P^T o (dP^T - Delta), 32 columns at a time, packed over the dP^T columns
+      // already read (half h of the packed values lands on columns of half 0)
       if (!wait_all(&bars->dp_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      {
-        uint32_t dr[2][32];
-        ld64(lane_addr + 128 + cb, dr);
-        uint32_t dd[32];
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(del_st + cc);
-          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-          float ds[4];
+      for (int hc = 0; hc < 64; hc += 32) {
+        uint32_t dr[32];
+        ptx::tmem_ld32(lane_addr + 128 + cb + hc, dr);
+        ptx::tmem_wait_ld_regs(dr);
+        uint32_t dd[16];
+        if (t.full) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int col = cc + u;
-            const bool vis = cb + col >= ilo && cb + col <= ihi;
-            const float dp = __uint_as_float(dr[col >> 5][col & 31]);
-            ds[u] = vis ? p[col] * (dp - dl[u]) : 0.f;
+          for (int cc = 0; cc < 32; cc += 2) {
+            const float2 d2 = *reinterpret_cast<const float2*>(del_st + hc + cc);
+            // dP - Delta as an exact fma with -1, then P * (dP - Delta)
+            const uint64_t tt = ptx::ffma2(ptx::f2_pack(d2.x, d2.y), neg1x2,
+                                           ptx::f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])));
+            float ds0, ds1;
+            ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p[hc + cc], p[hc + cc + 1]), tt), ds0, ds1);
+            dd[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
           }
-          dd[cc / 2] = ptx::pack_bf16x2(ds[0], ds[1]);
-          dd[cc / 2 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            const int col = cb + hc + cc;
+            const bool v0 = col >= ilo && col <= ihi, v1 = col + 1 >= ilo && col + 1 <= ihi;
+            const float ds0 = v0 ? p[hc + cc] * (__uint_as_float(dr[cc]) - del_st[hc + cc]) : 0.f;
+            const float ds1 = v1 ? p[hc + cc + 1] * (__uint_as_float(dr[cc + 1]) - del_st[hc + cc + 1]) : 0.f;
+            dd[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
+          }
         }
-        ptx::tmem_st32(lane_addr + 128 + cb, dd);  // dS^T over the first 32 of this warpgroup's dP^T columns
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->ds_full);
+        ptx::tmem_st16(lane_addr + 128 + cb + hc / 2, dd);
       }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->ds_full);
       ++j;
     }
     // ------------------------------------------------------------ dK / dV epilogue
@@ -767,6 +787,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       delta = a.delta[col];
     }
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nl2x2 = ptx::f2_pack(nlse2, nlse2);
+    const uint64_t nd2x2 = ptx::f2_pack(-delta, -delta);
     int seg = seg_begin, j0 = 0, j = 0;
     KvTile t;
     bool ok = true;
@@ -787,41 +809,70 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         }
       }
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
-      // phase 1: P from S, then release S for the next tile
+      // phase 1: P from S (32 columns at a time), then release S for the next tile
       if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
       float p[64];
-      {
-        uint32_t sr[2][32];
-        ld64(lane_addr + cb, sr);
+      const bool fast = t.full && nq_tile == kTileRows;  // every pair visible: no per-column mask
 #pragma unroll
-        for (int col = 0; col < 64; ++col) {
-          const bool vis = cb + col >= ilo && cb + col <= ihi;
-          p[col] = vis ? ptx::ex2_approx(fmaf(__uint_as_float(sr[col >> 5][col & 31]), sl2, nlse2)) : 0.f;
+      for (int hc = 0; hc < 64; hc += 32) {
+        uint32_t sr[32];
+        ptx::tmem_ld32(lane_addr + cb + hc, sr);
+        ptx::tmem_wait_ld_regs(sr);
+        if (fast) {
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            float a0, a1;
+            ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])),
+                                      sl2x2, nl2x2), a0, a1);
+            p[hc + cc] = ptx::ex2_approx(a0);
+            p[hc + cc + 1] = ptx::ex2_approx(a1);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const int col = cb + hc + cc;
+            const bool vis = col >= ilo && col <= ihi;
+            p[hc + cc] = vis ? ptx::ex2_approx(fmaf(__uint_as_float(sr[cc]), sl2, nlse2)) : 0.f;
+          }
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->s_free);
-      // phase 2: dS = P o (dP - Delta), written over dP
+      // phase 2: dS = P o (dP - Delta), 32 columns at a time, packed over the dP columns
+      // already read
       if (!wait_all(&bars->dp_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      {
-        uint32_t dr[2][32];
-        ld64(lane_addr + 128 + cb, dr);
-        uint32_t dd[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c0 = 2 * i, c1 = 2 * i + 1;
-          const bool v0 = cb + c0 >= ilo && cb + c0 <= ihi, v1 = cb + c1 >= ilo && cb + c1 <= ihi;
-          const float ds0 = v0 ? p[c0] * (__uint_as_float(dr[c0 >> 5][c0 & 31]) - delta) : 0.f;
-          const float ds1 = v1 ? p[c1] * (__uint_as_float(dr[c1 >> 5][c1 & 31]) - delta) : 0.f;
-          dd[i] = ptx::pack_bf16x2(ds0, ds1);
+      for (int hc = 0; hc < 64; hc += 32) {
+        uint32_t dr[32];
+        ptx::tmem_ld32(lane_addr + 128 + cb + hc, dr);
+        ptx::tmem_wait_ld_regs(dr);
+        uint32_t dd[16];
+        if (fast) {
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            const uint64_t tt = ptx::fadd2(ptx::f2_pack(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])),
+                                           nd2x2);
+            float ds0, ds1;
+            ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p[hc + cc], p[hc + cc + 1]), tt), ds0, ds1);
+            dd[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            const int col = cb + hc + cc;
+            const bool v0 = col >= ilo && col <= ihi, v1 = col + 1 >= ilo && col + 1 <= ihi;
+            const float ds0 = v0 ? p[hc + cc] * (__uint_as_float(dr[cc]) - delta) : 0.f;
+            const float ds1 = v1 ? p[hc + cc + 1] * (__uint_as_float(dr[cc + 1]) - delta) : 0.f;
+            dd[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
+          }
         }
-        ptx::tmem_st32(lane_addr + 128 + cb, dd);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->ds_full);
+        ptx::tmem_st16(lane_addr + 128 + cb + hc / 2, dd);
       }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->ds_full);
       ++j;
     }
     // ------------------------------------------------------------ dQ epilogue

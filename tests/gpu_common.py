@@ -31,7 +31,8 @@ def max_err(gpu, ref):
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, (g.shape, r.shape)
     both_inf = np.isneginf(g) & np.isneginf(r)
-    d = np.abs(np.where(both_inf, 0.0, g - r))
+    with np.errstate(invalid="ignore"):  # -inf - -inf where both are -inf: masked by both_inf
+        d = np.abs(np.where(both_inf, 0.0, g - r))
     return float(np.nan_to_num(d, nan=np.inf).max()) if d.size else 0.0
 
 
