@@ -17,12 +17,15 @@
 //               columns of its S buffer with tcgen05.st.  O is rescaled in
 //               TMEM only when the max grew by more than 2^8 (otherwise the
 //               stale max is kept; the final normalisation absorbs it).
-//   warp 8      TMA producer: Q0/Q1 once, K and V tiles (128 keys) in 2-stage
-//               rings of 128B-swizzled shared-memory buffers.  (Warps 8..11 form
-//               the third warpgroup, which gives registers to the softmax ones.)
+//   warp 8      TMA producer: Q0/Q1 once, K and V tiles (128 keys) in a 2-stage
+//               ring of 128B-swizzled shared-memory buffers, one barrier per
+//               stage.  (Warps 8..11 form the third warpgroup, which gives
+//               registers to the softmax ones.)
 //   warp 9      MMA issuer (one thread), ping-pong order per key tile j:
 //                 S0 = Q0 K_j^T | O1 += P1 V_{j-1} | S1 = Q1 K_j^T | O0 += P0 V_j
-//               so each softmax overlaps the other tile's two products.
+//               so each softmax overlaps the other tile's two products.  The
+//               pipe queues about one MMA, so the issuer does no schedule
+//               walking in the loop and at most one barrier wait between products.
 //               P is the A operand straight from TMEM (M=128 lanes, two bf16 per
 //               column); V is the B operand from shared memory (MN-major).
 // TMEM: S0/P0 cols 0..127, O0 128..255, S1/P1 256..383, O1 384..511.
@@ -45,14 +48,15 @@ constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;         // warps 10, 11 only rebalance registers
 // Register split (launch: 384 x 168 = 64512): the producer/MMA warpgroup drops to
-// 56, the two softmax warpgroups rise to 224: 128*56 + 256*224 = 64512.
-constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 224;
+// 64, the two softmax warpgroups rise to 216: 128*64 + 256*216 = 63488 <= 64512.
+constexpr int kRegsLow = 64;
+constexpr int kRegsHigh = 216;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s when draining after an abort
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kSegCap = 128;                  // segments per group kept in shared memory
 
 template <int D>
 struct Layout {
@@ -61,15 +65,16 @@ struct Layout {
   static constexpr int kK = kQ + 2 * kTile;  // 2 stages
   static constexpr int kV = kK + 2 * kTile;  // 2 stages
   static constexpr int kBar = kV + 2 * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kSeg = kBar + 256;  // the group's key/value segments (up to kSegCap)
+  static constexpr int kBytes = kSeg + kSegCap * (int)sizeof(KSeg);
   // One CTA per SM: TMEM (512 columns) is allocated whole.
   static constexpr int kSmemRequest = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], v_full[2];
-  uint64_t k_empty[2], v_empty[2];
+  uint64_t kv_full[2];   // K and V tile of a stage landed
+  uint64_t kv_empty[2];  // every product reading the stage completed
   uint64_t s_full[2];  // per query tile
   uint64_t p_full[2];  // per query tile
   uint64_t o_done;
@@ -100,36 +105,77 @@ __device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t
   }
 }
 
-// Next key/value tile with any visible pair for the CTA's query span.  Identical in every role.
-__device__ __forceinline__ bool next_tile(const Schedule& s, const SpanCtx& c, int causal, int docs,
-                                          int seg_end, int& seg, int& j0, KvTile& t) {
-  while (seg < seg_end) {
-    const int32_t k_row0 = s.s[seg].k_row0, nk_seg = s.s[seg].nk;
-    const int32_t poff = s.s[seg].pos_off, pst = s.s[seg].pos_stride;
-    if (j0 >= nk_seg) {
-      ++seg;
-      j0 = 0;
-      continue;
+// Visible key/value tiles of one segment for the CTA's query span: tile indices
+// [lo, hi) of the segment's BN-key tiles.  Positions grow with the tile index, so
+// the tiles after the queries (causal) or after the last query's document end form
+// a suffix, and the tiles before the first query's document start form a prefix.
+__device__ __forceinline__ void seg_range(const KSeg& sg, const SpanCtx& c, int causal, int docs,
+                                          int& lo, int& hi) {
+  const int64_t step = (int64_t)sg.pos_stride * BN;  // position advance per tile
+  hi = (sg.nk + BN - 1) / BN;
+  if (causal) {  // pk_lo(i) <= pq_hi
+    const int64_t d = c.pq_hi - sg.pos_off;
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+  }
+  if (docs) {  // pk_lo(i) < en_hi
+    const int64_t d = c.en_hi - 1 - sg.pos_off;
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+  }
+  lo = 0;
+  if (docs && hi > 0) {  // pk_hi(i) >= st_lo: start from a lower bound, then step forward
+    const int64_t d = c.st_lo - sg.pos_off;
+    if (d > 0) lo = (int)max((int64_t)0, (d / sg.pos_stride - (BN - 1)) / BN);
+    while (lo < hi) {
+      const int nk = min(BN, sg.nk - lo * BN);
+      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * BN + nk - 1) >= c.st_lo) break;
+      ++lo;
     }
-    const int nk = min(BN, nk_seg - j0);
-    const int64_t pk_lo = (int64_t)poff + (int64_t)pst * j0;
-    const int64_t pk_hi = pk_lo + (int64_t)pst * (nk - 1);
-    const int jcur = j0;
-    j0 += BN;
-    if ((causal && pk_lo > c.pq_hi) || (docs && pk_lo >= c.en_hi)) {
-      ++seg;  // this and every later tile of the segment lie after the queries
-      j0 = 0;
-      continue;
+  }
+  if (lo > hi) lo = hi;
+}
+
+// Walks the visible key/value tiles of the CTA's segments in order.  Identical in every role.
+struct TileIter {
+  const KSeg* segs;
+  int nseg, si, i, hi;
+};
+
+__device__ __forceinline__ void iter_init(TileIter& it, const KSeg* segs, int nseg, const SpanCtx& c,
+                                          int causal, int docs) {
+  it.segs = segs;
+  it.nseg = nseg;
+  it.si = 0;
+  it.i = it.hi = 0;
+  if (nseg > 0) seg_range(segs[0], c, causal, docs, it.i, it.hi);
+}
+
+__device__ __forceinline__ bool iter_next(TileIter& it, const SpanCtx& c, int causal, int docs, KvTile& t) {
+  while (it.si < it.nseg) {
+    if (it.i < it.hi) {
+      const KSeg sg = it.segs[it.si];
+      const int j0 = it.i * BN;
+      t.k_row = sg.k_row0 + j0;
+      t.nk = min(BN, sg.nk - j0);
+      t.pk_lo = (int64_t)sg.pos_off + (int64_t)sg.pos_stride * j0;
+      t.pk_hi = t.pk_lo + (int64_t)sg.pos_stride * (t.nk - 1);
+      t.kstride = sg.pos_stride;
+      ++it.i;
+      return true;
     }
-    if (docs && pk_hi < c.st_lo) continue;  // before the first query's document
-    t.k_row = k_row0 + jcur;
-    t.nk = nk;
-    t.pk_lo = pk_lo;
-    t.pk_hi = pk_hi;
-    t.kstride = pst;
-    return true;
+    if (++it.si < it.nseg) seg_range(it.segs[it.si], c, causal, docs, it.i, it.hi);
   }
   return false;
+}
+
+__device__ __forceinline__ int count_tiles(const KSeg* segs, int nseg, const SpanCtx& c, int causal,
+                                           int docs) {
+  int n = 0;
+  for (int si = 0; si < nseg; ++si) {
+    int lo, hi;
+    seg_range(segs[si], c, causal, docs, lo, hi);
+    n += hi - lo;
+  }
+  return n;
 }
 
 // Every (row, key) pair of the tile visible for this query span (no mask needed)?
@@ -182,13 +228,17 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
     span_init(cta, a, lo, lo + (int64_t)qpos_st * (nq0 + nq1 - 1));
   }
 
+  // The group's segments, read at every tile by every role: shared memory when they fit.
+  const int nseg = seg_end - seg_begin;
+  KSeg* seg_sm = reinterpret_cast<KSeg*>(smem + L::kSeg);
+  const KSeg* segs = nseg <= kSegCap ? seg_sm : &s.s[seg_begin];
+  if (nseg <= kSegCap)
+    for (int i = threadIdx.x; i < nseg; i += kThreads) seg_sm[i] = s.s[seg_begin + i];
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&bars->k_full[i], 1);
-      ptx::mbar_init(&bars->v_full[i], 1);
-      ptx::mbar_init(&bars->k_empty[i], 1);
-      ptx::mbar_init(&bars->v_empty[i], 1);
+      ptx::mbar_init(&bars->kv_full[i], 1);
+      ptx::mbar_init(&bars->kv_empty[i], 1);
       ptx::mbar_init(&bars->s_full[i], 1);
       ptx::mbar_init(&bars->p_full[i], 128);
     }
@@ -221,42 +271,34 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
         for (int r = 0; r < D / 64; ++r)
           ptx::tma_load_2d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
                            h * D + r * 64, q_row0 + i0 + w * BM);
-      int seg = seg_begin, j0 = 0, j = 0;
+      TileIter it;
+      iter_init(it, segs, nseg, cta, causal, docs);
+      int j = 0;
       KvTile t;
-      int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
-      while (!*abort_flag && next_tile(s, cta, causal, docs, seg_end, seg, j0, t)) {
+      int issued[2] = {0, 0};
+      while (!*abort_flag && iter_next(it, cta, causal, docs, t)) {
         const int st = j & 1;
-        if (j >= 2 && !ptx::mbar_wait_bounded(&bars->k_empty[st], ((j >> 1) - 1) & 1, abort_flag,
+        if (j >= 2 && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j >> 1) - 1) & 1, abort_flag,
                                               a.err, kWaitNs))
           break;
-        ptx::mbar_arrive_expect_tx(&bars->k_full[st], L::kTile);
+        ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::kTile);
 #pragma unroll
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->k_full[st],
+        for (int r = 0; r < D / 64; ++r) {
+          ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
                            hk * D + r * 64, t.k_row);
-        issued_k[st] = j + 1;
-        if (j >= 2 && !ptx::mbar_wait_bounded(&bars->v_empty[st], ((j >> 1) - 1) & 1, abort_flag,
-                                              a.err, kWaitNs))
-          break;
-        ptx::mbar_arrive_expect_tx(&bars->v_full[st], L::kTile);
-#pragma unroll
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->v_full[st],
+          ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
                            hk * D + r * 64, t.k_row);
-        issued_v[st] = j + 1;
+        }
+        issued[st] = j + 1;
         ++j;
       }
       if (*abort_flag) {
         // drain: wait (bounded) for this CTA's own copies still in flight
         (void)ptx::mbar_wait_bounded(&bars->q_full, 0, nullptr, nullptr, kDrainNs);
-        for (int st = 0; st < 2; ++st) {
-          if (issued_k[st] > 0)
-            (void)ptx::mbar_wait_bounded(&bars->k_full[st], ((issued_k[st] - 1) >> 1) & 1, nullptr,
+        for (int st = 0; st < 2; ++st)
+          if (issued[st] > 0)
+            (void)ptx::mbar_wait_bounded(&bars->kv_full[st], ((issued[st] - 1) >> 1) & 1, nullptr,
                                          nullptr, kDrainNs);
-          if (issued_v[st] > 0)
-            (void)ptx::mbar_wait_bounded(&bars->v_full[st], ((issued_v[st] - 1) >> 1) & 1, nullptr,
-                                         nullptr, kDrainNs);
-        }
       }
     }
     __syncwarp();
@@ -280,45 +322,56 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
           ptx::mma_bf16_ts(tmem + w * 256 + 128, tmem + w * 256 + kk * 8,
                            desc_v_mnmajor<D>(v_addr, kk), idesc_pv, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = ptx::mbar_wait_bounded(&bars->q_full, 0, abort_flag, a.err, kWaitNs);
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
+      };
+      // The issuing thread stalls at each tcgen05.mma until the pipe accepts it, so
+      // every gap between two products holds at most one barrier wait and no
+      // schedule walking (the tile count is known up front).
+      const int n = count_tiles(segs, nseg, cta, causal, docs);
+      bool ok = wait(&bars->q_full, 0);
       bool any = false;
-      if (ok) {
-        int seg = seg_begin, j0 = 0, j = 0;
-        KvTile t;
-        bool more = next_tile(s, cta, causal, docs, seg_end, seg, j0, t);
-        while (true) {
+      if (ok && n > 0) {
+        ok = wait(&bars->kv_full[0], 0);
+        if (ok) {  // S0 = Q0 K_0^T
+          ptx::tc_fence_after();
+          qk(0, 0);
+          ptx::tc_commit(&bars->s_full[0]);
+          any = true;
+        }
+        for (int j = 0; ok && j < n; ++j) {
           const int st = j & 1;
-          if (more) {  // S0 = Q0 K_j^T
-            if (!ptx::mbar_wait_bounded(&bars->k_full[st], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
-            ptx::tc_fence_after();
-            qk(0, st);
-            ptx::tc_commit(&bars->s_full[0]);
-            any = true;
-          }
           if (has1 && j >= 1) {  // O1 += P1 V_{j-1}
-            const int jp = j - 1, stp = jp & 1;
-            if (!ptx::mbar_wait_bounded(&bars->p_full[1], jp & 1, abort_flag, a.err, kWaitNs)) break;
-            if (!ptx::mbar_wait_bounded(&bars->v_full[stp], (jp >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
+            const int stp = (j - 1) & 1;
+            if (!(ok = wait(&bars->p_full[1], (j - 1) & 1))) break;
+            ptx::tc_fence_after();
+            pv(1, stp, j - 1 > 0);
+            ptx::tc_commit(&bars->kv_empty[stp]);
+          }
+          if (has1) {  // S1 = Q1 K_j^T
+            qk(1, st);
+            ptx::tc_commit(&bars->s_full[1]);
+          }
+          // O0 += P0 V_j
+          if (!(ok = wait(&bars->p_full[0], j & 1))) break;
+          ptx::tc_fence_after();
+          pv(0, st, j > 0);
+          if (!has1) ptx::tc_commit(&bars->kv_empty[st]);
+          if (j + 1 < n) {  // S0 = Q0 K_{j+1}^T
+            const int st1 = (j + 1) & 1;
+            if (!(ok = wait(&bars->kv_full[st1], ((j + 1) >> 1) & 1))) break;
+            ptx::tc_fence_after();
+            qk(0, st1);
+            ptx::tc_commit(&bars->s_full[0]);
+          }
+        }
+        if (ok && has1) {  // O1 += P1 V_{n-1}
+          const int jp = n - 1, stp = jp & 1;
+          if (wait(&bars->p_full[1], jp & 1)) {
             ptx::tc_fence_after();
             pv(1, stp, jp > 0);
-            ptx::tc_commit(&bars->v_empty[stp]);
+            ptx::tc_commit(&bars->kv_empty[stp]);
           }
-          if (more) {
-            if (has1) {  // S1 = Q1 K_j^T
-              qk(1, st);
-              ptx::tc_commit(&bars->s_full[1]);
-            }
-            ptx::tc_commit(&bars->k_empty[st]);
-            // O0 += P0 V_j
-            if (!ptx::mbar_wait_bounded(&bars->p_full[0], j & 1, abort_flag, a.err, kWaitNs)) break;
-            if (!ptx::mbar_wait_bounded(&bars->v_full[st], (j >> 1) & 1, abort_flag, a.err, kWaitNs)) break;
-            ptx::tc_fence_after();
-            pv(0, st, j > 0);
-            if (!has1) ptx::tc_commit(&bars->v_empty[st]);
-          }
-          if (!more) break;
-          ++j;
-          more = next_tile(s, cta, causal, docs, seg_end, seg, j0, t);
         }
       }
       // o_done: every MMA of this CTA has completed (also the TMEM release condition)
@@ -349,14 +402,15 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       const float sl2 = a.scale_log2;
       const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       float m = -INFINITY, l = 0.f;
-      int seg = seg_begin, j0 = 0, j = 0;
+      TileIter it;
+      iter_init(it, segs, nseg, cta, causal, docs);
+      int j = 0;
       KvTile t;
       auto wwait = [&](uint64_t* bar, uint32_t par) {
         bool ok = ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
         return __all_sync(0xffffffffu, ok);
       };
-      while (__all_sync(0xffffffffu, *abort_flag == 0) &&
-             next_tile(s, cta, causal, docs, seg_end, seg, j0, t)) {
+      while (__all_sync(0xffffffffu, *abort_flag == 0) && iter_next(it, cta, causal, docs, t)) {
         const bool full = tile_full(mine, t, causal, docs);
         int ilo = 0, ihi = BN - 1;
         if (!full) {
