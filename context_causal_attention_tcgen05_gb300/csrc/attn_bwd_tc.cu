@@ -66,6 +66,7 @@ constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * D * 2;  // 32 KB: [128 rows][128 bf16], two 64-column regions
+constexpr int kSegCap = 128;                   // segments per group kept in shared memory
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
   // K-major, 128B swizzle: K step of 16 bf16 = 32 bytes inside a 64-column (16 KB) region.
@@ -116,7 +117,8 @@ struct ALayout {
   static constexpr int kDO = kQ + A_QST * kTileBytes;   // A_QST stages
   static constexpr int kLse = kDO + A_QST * kTileBytes;  // A_QST x (128 lse, 128 Delta) fp32
   static constexpr int kBar = kLse + A_QST * 2 * kTileRows * 4;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kSeg = kBar + 256;  // the group's query runs (up to kSegCap)
+  static constexpr int kBytes = kSeg + kSegCap * (int)sizeof(KSeg);
   static constexpr int kSmemRequest = kBytes + 1024;
 };
 
@@ -146,39 +148,61 @@ struct KeyCtx {
   int G, hk;
 };
 
-// Next query tile (over the G query heads, then the query runs) that sees some key of the tile.
-__device__ __forceinline__ bool next_qtile(const Schedule& s, const KeyCtx& c, int seg_begin,
-                                           int seg_end, int& hh, int& seg, int& i0, QTile& t) {
-  while (hh < c.G) {
-    if (seg >= seg_end) {
-      ++hh;
-      seg = seg_begin;
-      i0 = 0;
+// Walks the query tiles that see some key of the CTA's key tile: the G query heads
+// of the key/value head, each over the query runs in order.  Identical in every role.
+struct QIter {
+  const KSeg* segs;
+  int nseg, hh, si, i, hi;
+};
+
+__device__ __forceinline__ void qiter_init(QIter& it, const KSeg* segs, int nseg, const KeyCtx& c) {
+  it.segs = segs;
+  it.nseg = nseg;
+  it.hh = 0;
+  it.si = 0;
+  it.i = it.hi = 0;
+  if (nseg > 0) query_tile_range(segs[0], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
+}
+
+__device__ __forceinline__ bool qiter_next(QIter& it, const KeyCtx& c, QTile& t) {
+  while (it.hh < c.G) {
+    if (it.si < it.nseg && it.i < it.hi) {
+      const KSeg sg = it.segs[it.si];
+      const int i0 = it.i * kTileRows;
+      const int nq = min(kTileRows, sg.nk - i0);
+      const int64_t pq_lo = (int64_t)sg.pos_off + (int64_t)sg.pos_stride * i0;
+      const int64_t pq_hi = pq_lo + (int64_t)sg.pos_stride * (nq - 1);
+      t.q_row = sg.k_row0 + i0;
+      t.nq = nq;
+      t.pq_lo = pq_lo;
+      t.qstride = sg.pos_stride;
+      t.h = c.hk * c.G + it.hh;
+      t.full = (nq == kTileRows) && (c.causal ? pq_lo >= c.pk_hi : 1) && !c.docs;
+      if (c.docs && c.causal) t.full = (nq == kTileRows) && pq_lo >= c.pk_hi && c.en_lo > pq_hi;
+      ++it.i;
+      return true;
+    }
+    if (it.si < it.nseg && ++it.si < it.nseg) {
+      query_tile_range(it.segs[it.si], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
       continue;
     }
-    const int32_t q_row0 = s.s[seg].k_row0, nq_seg = s.s[seg].nk;
-    const int32_t poff = s.s[seg].pos_off, pst = s.s[seg].pos_stride;
-    if (i0 >= nq_seg) {
-      ++seg;
-      i0 = 0;
-      continue;
+    if (++it.hh < c.G) {
+      it.si = 0;
+      it.i = it.hi = 0;
+      if (it.nseg > 0) query_tile_range(it.segs[0], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
     }
-    const int nq = min(kTileRows, nq_seg - i0);
-    const int64_t pq_lo = (int64_t)poff + (int64_t)pst * i0;
-    const int64_t pq_hi = pq_lo + (int64_t)pst * (nq - 1);
-    const int icur = i0;
-    i0 += kTileRows;
-    if (c.causal && pq_hi < c.pk_lo) continue;  // every query before every key
-    t.q_row = q_row0 + icur;
-    t.nq = nq;
-    t.pq_lo = pq_lo;
-    t.qstride = pst;
-    t.h = c.hk * c.G + hh;
-    t.full = (nq == kTileRows) && (c.causal ? pq_lo >= c.pk_hi : 1) && !c.docs;
-    if (c.docs && c.causal) t.full = (nq == kTileRows) && pq_lo >= c.pk_hi && c.en_lo > pq_hi;
-    return true;
   }
   return false;
+}
+
+__device__ __forceinline__ int count_qtiles(const KSeg* segs, int nseg, const KeyCtx& c) {
+  int n = 0;
+  for (int si = 0; si < nseg; ++si) {
+    int lo, hi;
+    query_tile_range(segs[si], kTileRows, c.pk_lo, c.causal, lo, hi);
+    n += hi - lo;
+  }
+  return n * c.G;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -213,6 +237,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     doc_bounds(a.cu_seqlens, a.n_docs, c.pk_lo, &st, &c.en_lo);
   }
 
+  // The group's query runs, read at every tile by every role: shared memory when they fit.
+  const int nseg = seg_end - seg_begin;
+  KSeg* seg_sm = reinterpret_cast<KSeg*>(smem + L::kSeg);
+  const KSeg* segs = nseg <= kSegCap ? seg_sm : &s.s[seg_begin];
+  if (nseg <= kSegCap)
+    for (int i = threadIdx.x; i < nseg; i += kThreads) seg_sm[i] = s.s[seg_begin + i];
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->kv_full, 1);
     for (int i = 0; i < A_QST; ++i) {
@@ -254,11 +284,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
           ptx::tma_load_2d(smem + L::kV + r * 16384, &tm_v, &bars->kv_full, hk * D + r * 64, k_row0);
         }
       }
-      int hh = 0, seg = seg_begin, i0 = 0, j = 0;
+      QIter it;
+      qiter_init(it, segs, nseg, c);
+      int j = 0;
       QTile t;
       int issued[A_QST] = {0, 0};
-      while (__all_sync(0xffffffffu, *abort_flag == 0) &&
-             next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
+      while (__all_sync(0xffffffffu, *abort_flag == 0) && qiter_next(it, c, t)) {
         const int st = j % A_QST;
         if (j >= A_QST && !wait_all(&bars->q_empty[st], ((j / A_QST) - 1) & 1, abort_flag, a.err)) break;
         if (lane == 0) {
@@ -310,10 +341,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
             ptx::mma_bf16_ts(tmem + d, a_split(tmem + a_tmem, kk), desc_mn(b_addr, kk), id_kv,
                              (acc || kk > 0) ? 1u : 0u);
         };
+        const int n = count_qtiles(segs, nseg, c);  // no schedule walking between products
         if (wait(&bars->kv_full, 0)) {
-          int hh = 0, seg = seg_begin, i0 = 0, j = 0;
-          QTile t;
-          bool have = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+          int j = 0;
+          bool have = n > 0;
           if (have) {
             if (!wait(&bars->q_full[0], 0)) have = false;
             if (have) {
@@ -326,7 +357,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
             }
           }
           while (have) {
-            const bool more = next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t);
+            const bool more = j + 1 < n;
             const int st = j % A_QST, st1 = (j + 1) % A_QST;
             // dV += P^T dO once P^T is written back
             if (!wait(&bars->p_full, j & 1)) break;
@@ -375,11 +406,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nlog2e2 = ptx::f2_pack(-kLog2e, -kLog2e);
     const uint64_t neg1x2 = ptx::f2_pack(-1.f, -1.f);
-    int hh = 0, seg = seg_begin, i0 = 0, j = 0;
+    QIter it;
+    qiter_init(it, segs, nseg, c);
+    int j = 0;
     QTile t;
     bool ok = true;
-    while (__all_sync(0xffffffffu, *abort_flag == 0) &&
-           next_qtile(s, c, seg_begin, seg_end, hh, seg, i0, t)) {
+    while (__all_sync(0xffffffffu, *abort_flag == 0) && qiter_next(it, c, t)) {
       const int st = j % A_QST;
       int64_t hi = t.nq - 1, lo = 0;  // visible query columns of this key row: [lo, hi]
       if (r >= nk_tile) {
@@ -531,13 +563,14 @@ struct BLayout {
   static constexpr int kK = 0;                          // B_KST stages
   static constexpr int kV = kK + B_KST * kTileBytes;
   static constexpr int kBar = kV + B_KST * kTileBytes;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kSeg = kBar + 256;  // the group's key runs (up to kSegCap)
+  static constexpr int kBytes = kSeg + kSegCap * (int)sizeof(KSeg);
   static constexpr int kSmemRequest = kBytes + 1024;
 };
 
 struct BBars {
   uint64_t q_full;  // Q and dO copied into TMEM
-  uint64_t k_full[B_KST], v_full[B_KST], kv_empty[B_KST];
+  uint64_t kv_full[B_KST], kv_empty[B_KST];  // K and V tile of a stage landed / released
   uint64_t s_full, dp_full;  // S / dP of the current tile in TMEM
   uint64_t s_free;           // the softmax has read S
   uint64_t ds_full;          // dS written back
@@ -560,37 +593,55 @@ struct KvTile {
   int32_t full;
 };
 
-// Next key/value tile (128 keys) of the query group with any visible pair.
-__device__ __forceinline__ bool next_ktile(const Schedule& s, const TileCtx& c, int seg_end, int& seg,
-                                           int& j0, KvTile& t) {
-  while (seg < seg_end) {
-    const int32_t k_row0 = s.s[seg].k_row0, nk_seg = s.s[seg].nk;
-    const int32_t poff = s.s[seg].pos_off, pst = s.s[seg].pos_stride;
-    if (j0 >= nk_seg) {
-      ++seg;
-      j0 = 0;
-      continue;
+// Walks the key/value tiles (128 keys) of the query group with any visible pair.
+// Identical in every role.
+struct KIter {
+  const KSeg* segs;
+  int nseg, si, i, hi;
+};
+
+__device__ __forceinline__ void kiter_range(KIter& it, const TileCtx& c) {
+  key_tile_range(it.segs[it.si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, it.i, it.hi);
+}
+
+__device__ __forceinline__ void kiter_init(KIter& it, const KSeg* segs, int nseg, const TileCtx& c) {
+  it.segs = segs;
+  it.nseg = nseg;
+  it.si = 0;
+  it.i = it.hi = 0;
+  if (nseg > 0) kiter_range(it, c);
+}
+
+__device__ __forceinline__ bool kiter_next(KIter& it, const TileCtx& c, KvTile& t) {
+  while (it.si < it.nseg) {
+    if (it.i < it.hi) {
+      const KSeg sg = it.segs[it.si];
+      const int j0 = it.i * kTileRows;
+      const int nk = min(kTileRows, sg.nk - j0);
+      const int64_t pk_lo = (int64_t)sg.pos_off + (int64_t)sg.pos_stride * j0;
+      const int64_t pk_hi = pk_lo + (int64_t)sg.pos_stride * (nk - 1);
+      t.k_row = sg.k_row0 + j0;
+      t.nk = nk;
+      t.pk_lo = pk_lo;
+      t.kstride = sg.pos_stride;
+      t.full = (nk == kTileRows) && (!c.causal || pk_hi <= c.pq_lo) &&
+               (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo));
+      ++it.i;
+      return true;
     }
-    const int nk = min(kTileRows, nk_seg - j0);
-    const int64_t pk_lo = (int64_t)poff + (int64_t)pst * j0;
-    const int64_t pk_hi = pk_lo + (int64_t)pst * (nk - 1);
-    const int jcur = j0;
-    j0 += kTileRows;
-    if ((c.causal && pk_lo > c.pq_hi) || (c.docs && pk_lo >= c.en_hi)) {
-      ++seg;
-      j0 = 0;
-      continue;
-    }
-    if (c.docs && pk_hi < c.st_lo) continue;
-    t.k_row = k_row0 + jcur;
-    t.nk = nk;
-    t.pk_lo = pk_lo;
-    t.kstride = pst;
-    t.full = (nk == kTileRows) && (!c.causal || pk_hi <= c.pq_lo) &&
-             (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo));
-    return true;
+    if (++it.si < it.nseg) kiter_range(it, c);
   }
   return false;
+}
+
+__device__ __forceinline__ int count_ktiles(const KSeg* segs, int nseg, const TileCtx& c) {
+  int n = 0;
+  for (int si = 0; si < nseg; ++si) {
+    int lo, hi;
+    key_tile_range(segs[si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, lo, hi);
+    n += hi - lo;
+  }
+  return n;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -624,11 +675,16 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     doc_bounds(a.cu_seqlens, a.n_docs, c.pq_hi, &c.st_hi, &c.en_hi);
   }
 
+  // The group's key runs, read at every tile by every role: shared memory when they fit.
+  const int nseg = seg_end - seg_begin;
+  KSeg* seg_sm = reinterpret_cast<KSeg*>(smem + L::kSeg);
+  const KSeg* segs = nseg <= kSegCap ? seg_sm : &s.s[seg_begin];
+  if (nseg <= kSegCap)
+    for (int i = threadIdx.x; i < nseg; i += kThreads) seg_sm[i] = s.s[seg_begin + i];
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, kSoftmaxThreads);
     for (int i = 0; i < B_KST; ++i) {
-      ptx::mbar_init(&bars->k_full[i], 1);
-      ptx::mbar_init(&bars->v_full[i], 1);
+      ptx::mbar_init(&bars->kv_full[i], 1);
       ptx::mbar_init(&bars->kv_empty[i], 1);
     }
     ptx::mbar_init(&bars->s_full, 1);
@@ -658,32 +714,31 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
-        int seg = seg_begin, j0 = 0, j = 0;
+        KIter it;
+        kiter_init(it, segs, nseg, c);
+        int j = 0;
         KvTile t;
         int issued[B_KST] = {0, 0, 0};
-        while (!*abort_flag && next_ktile(s, c, seg_end, seg, j0, t)) {
+        while (!*abort_flag && kiter_next(it, c, t)) {
           const int st = j % B_KST;
           if (j >= B_KST && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j / B_KST) - 1) & 1, abort_flag,
                                                      a.err, kWaitNs))
             break;
-          ptx::mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-          for (int r = 0; r < D / 64; ++r)
-            ptx::tma_load_2d(smem + L::kK + st * kTileBytes + r * 16384, &tm_k, &bars->k_full[st],
+          ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * kTileBytes);
+          for (int r = 0; r < D / 64; ++r) {
+            ptx::tma_load_2d(smem + L::kK + st * kTileBytes + r * 16384, &tm_k, &bars->kv_full[st],
                              hk * D + r * 64, t.k_row);
-          ptx::mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-          for (int r = 0; r < D / 64; ++r)
-            ptx::tma_load_2d(smem + L::kV + st * kTileBytes + r * 16384, &tm_v, &bars->v_full[st],
+            ptx::tma_load_2d(smem + L::kV + st * kTileBytes + r * 16384, &tm_v, &bars->kv_full[st],
                              hk * D + r * 64, t.k_row);
+          }
           issued[st] = j + 1;
           ++j;
         }
         if (*abort_flag) {
           for (int st = 0; st < B_KST; ++st)
-            if (issued[st] > 0) {
-              const uint32_t par = ((issued[st] - 1) / B_KST) & 1;
-              (void)ptx::mbar_wait_bounded(&bars->k_full[st], par, nullptr, nullptr, kDrainNs);
-              (void)ptx::mbar_wait_bounded(&bars->v_full[st], par, nullptr, nullptr, kDrainNs);
-            }
+            if (issued[st] > 0)
+              (void)ptx::mbar_wait_bounded(&bars->kv_full[st], ((issued[st] - 1) / B_KST) & 1, nullptr,
+                                           nullptr, kDrainNs);
         }
       }
       __syncwarp();
@@ -701,35 +756,29 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
           for (int kk = 0; kk < D / 16; ++kk)
             ptx::mma_bf16_ts(tmem + d, tmem + a_tmem + kk * 8, desc_k(b_addr, kk), id_s, kk > 0);
         };
-        if (wait(&bars->q_full, 0)) {
+        // Issue order S_{j+1}, dQ_j, dP_{j+1}; each gap between two products holds one
+        // barrier wait (tile j+2's K/V is waited for one tile ahead) and no schedule walking.
+        const int n = count_ktiles(segs, nseg, c);
+        if (n > 0 && wait(&bars->q_full, 0) && wait(&bars->kv_full[0], 0)) {
           ptx::tc_fence_after();
-          int seg = seg_begin, j0 = 0, j = 0;
-          KvTile t;
-          bool have = next_ktile(s, c, seg_end, seg, j0, t);
-          if (have) {
-            have = wait(&bars->k_full[0], 0) && wait(&bars->v_full[0], 0);
-            if (have) {
-              ptx::tc_fence_after();
-              scores(0, 384, sbase + L::kK);
-              ptx::tc_commit(&bars->s_full);
-              scores(128, 448, sbase + L::kV);
-              ptx::tc_commit(&bars->dp_full);
-              any = true;
-            }
-          }
-          while (have) {
-            const bool more = next_ktile(s, c, seg_end, seg, j0, t);
-            const int st = j % B_KST, st1 = (j + 1) % B_KST, par1 = ((j + 1) / B_KST) & 1;
+          scores(0, 384, sbase + L::kK);
+          ptx::tc_commit(&bars->s_full);
+          scores(128, 448, sbase + L::kV);
+          ptx::tc_commit(&bars->dp_full);
+          any = true;
+          bool ok = n < 2 || wait(&bars->kv_full[1 % B_KST], (1 / B_KST) & 1);
+          for (int j = 0; ok && j < n; ++j) {
+            const int st = j % B_KST, st1 = (j + 1) % B_KST;
+            const bool more = j + 1 < n;
             // next tile's S once the softmax has read this tile's S
             if (more) {
-              if (!wait(&bars->s_free, j & 1)) break;
-              if (!wait(&bars->k_full[st1], par1)) break;
+              if (!(ok = wait(&bars->s_free, j & 1))) break;
               ptx::tc_fence_after();
               scores(0, 384, sbase + L::kK + st1 * kTileBytes);
               ptx::tc_commit(&bars->s_full);
             }
             // dQ += dS K once dS is written back (dS: two warpgroup halves of 64 keys)
-            if (!wait(&bars->ds_full, j & 1)) break;
+            if (!(ok = wait(&bars->ds_full, j & 1))) break;
             ptx::tc_fence_after();
             {
               const uint32_t k_addr = sbase + L::kK + st * kTileBytes;
@@ -741,13 +790,10 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
             ptx::tc_commit(&bars->kv_empty[st]);
             // next tile's dP (reuses the dP columns after dQ has read dS)
             if (more) {
-              if (!wait(&bars->v_full[st1], par1)) break;
-              ptx::tc_fence_after();
               scores(128, 448, sbase + L::kV + st1 * kTileBytes);
               ptx::tc_commit(&bars->dp_full);
+              if (j + 2 < n) ok = wait(&bars->kv_full[(j + 2) % B_KST], ((j + 2) / B_KST) & 1);
             }
-            ++j;
-            have = more;
           }
         }
         if (any) {
@@ -789,10 +835,12 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nl2x2 = ptx::f2_pack(nlse2, nlse2);
     const uint64_t nd2x2 = ptx::f2_pack(-delta, -delta);
-    int seg = seg_begin, j0 = 0, j = 0;
+    KIter it;
+    kiter_init(it, segs, nseg, c);
+    int j = 0;
     KvTile t;
     bool ok = true;
-    while (__all_sync(0xffffffffu, *abort_flag == 0) && next_ktile(s, c, seg_end, seg, j0, t)) {
+    while (__all_sync(0xffffffffu, *abort_flag == 0) && kiter_next(it, c, t)) {
       int64_t hi = t.nk - 1, lo = 0;
       if (!row_valid) {
         hi = -1;

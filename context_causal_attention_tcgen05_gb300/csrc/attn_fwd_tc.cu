@@ -105,33 +105,10 @@ __device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t
   }
 }
 
-// Visible key/value tiles of one segment for the CTA's query span: tile indices
-// [lo, hi) of the segment's BN-key tiles.  Positions grow with the tile index, so
-// the tiles after the queries (causal) or after the last query's document end form
-// a suffix, and the tiles before the first query's document start form a prefix.
+// Visible key/value tiles [lo, hi) of one segment for the CTA's query span.
 __device__ __forceinline__ void seg_range(const KSeg& sg, const SpanCtx& c, int causal, int docs,
                                           int& lo, int& hi) {
-  const int64_t step = (int64_t)sg.pos_stride * BN;  // position advance per tile
-  hi = (sg.nk + BN - 1) / BN;
-  if (causal) {  // pk_lo(i) <= pq_hi
-    const int64_t d = c.pq_hi - sg.pos_off;
-    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
-  }
-  if (docs) {  // pk_lo(i) < en_hi
-    const int64_t d = c.en_hi - 1 - sg.pos_off;
-    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
-  }
-  lo = 0;
-  if (docs && hi > 0) {  // pk_hi(i) >= st_lo: start from a lower bound, then step forward
-    const int64_t d = c.st_lo - sg.pos_off;
-    if (d > 0) lo = (int)max((int64_t)0, (d / sg.pos_stride - (BN - 1)) / BN);
-    while (lo < hi) {
-      const int nk = min(BN, sg.nk - lo * BN);
-      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * BN + nk - 1) >= c.st_lo) break;
-      ++lo;
-    }
-  }
-  if (lo > hi) lo = hi;
+  key_tile_range(sg, BN, c.pq_hi, c.st_lo, c.en_hi, causal, docs, lo, hi);
 }
 
 // Walks the visible key/value tiles of the CTA's segments in order.  Identical in every role.

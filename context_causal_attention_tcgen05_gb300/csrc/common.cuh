@@ -202,6 +202,56 @@ __device__ __forceinline__ void doc_bounds(const int32_t* cu, int32_t n_docs, in
   *end = __ldg(cu + lo + 1);
 }
 
+// Tiles of `tile` rows over one schedule segment.  Positions grow with the row
+// index (pos_stride >= 1), so each visibility test below holds for a prefix or a
+// suffix of the segment's tiles and a range is found without walking them.
+
+// Key tiles [lo, hi) of segment sg holding a key that some query of a span can
+// see: not after the span's last query pq_hi (causal), not at or after the end
+// en_hi of that query's document, not wholly before the start st_lo of the first
+// query's document (documents only).
+__device__ __forceinline__ void key_tile_range(const KSeg& sg, int tile, int64_t pq_hi, int64_t st_lo,
+                                               int64_t en_hi, int causal, int docs, int& lo, int& hi) {
+  const int64_t step = (int64_t)sg.pos_stride * tile;  // position advance per tile
+  hi = (sg.nk + tile - 1) / tile;
+  if (causal) {  // first key of the tile <= pq_hi
+    const int64_t d = pq_hi - sg.pos_off;
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+  }
+  if (docs) {  // first key of the tile < en_hi
+    const int64_t d = en_hi - 1 - sg.pos_off;
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+  }
+  lo = 0;
+  if (docs && hi > 0) {  // last key of the tile >= st_lo: a lower bound, then step forward
+    const int64_t d = st_lo - sg.pos_off;
+    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (d / sg.pos_stride - (tile - 1)) / tile));
+    while (lo < hi) {
+      const int n = min(tile, sg.nk - lo * tile);
+      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= st_lo) break;
+      ++lo;
+    }
+  }
+  if (lo > hi) lo = hi;
+}
+
+// Query tiles [lo, hi) of segment sg holding a query at or after key position
+// pk_lo (causal); every tile otherwise.
+__device__ __forceinline__ void query_tile_range(const KSeg& sg, int tile, int64_t pk_lo, int causal,
+                                                 int& lo, int& hi) {
+  hi = (sg.nk + tile - 1) / tile;
+  lo = 0;
+  if (causal) {  // last query of the tile >= pk_lo: a lower bound, then step forward
+    const int64_t d = pk_lo - sg.pos_off;
+    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (d / sg.pos_stride - (tile - 1)) / tile));
+    while (lo < hi) {
+      const int n = min(tile, sg.nk - lo * tile);
+      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= pk_lo) break;
+      ++lo;
+    }
+  }
+}
+
 // Locates unit u in a schedule: query group, query tile index, head.
 __device__ __forceinline__ void decode_unit(const Schedule& s, int tile_rows, int heads, int u,
                                             int* g_out, int* tile_out, int* h_out) {
