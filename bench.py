@@ -262,7 +262,26 @@ def bench_ours(args):
         ms = timed(lambda: cpa.cp_lse_merge(o1, l1, o2, l2, out=o1, lse=l1), reps)
         nbytes = 3 * o1.numel() * 4 + 3 * l1.numel() * 4
         out["lse_merge_f32_s8192_h32_d128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
-        del o1, o2, l1, l2
+        del o1, o2
+        b1 = torch.randn(S, H, D, device=dev).to(torch.bfloat16)
+        b2 = torch.randn(S, H, D, device=dev).to(torch.bfloat16)
+        ms = timed(lambda: cpa.cp_lse_merge(b1, l1, b2, l2, out=b1, lse=l1), reps)
+        nbytes = 3 * b1.numel() * 2 + 3 * l1.numel() * 4
+        out["lse_merge_bf16_s8192_h32_d128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
+        del b1, b2, l1, l2
+        # the same merges at the GQA ring shape (S=65536, H=32)
+        S4 = 65536
+        l1 = torch.randn(H, S4, device=dev)
+        l2 = torch.randn(H, S4, device=dev)
+        for name, dt, esz in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+            c1 = torch.randn(S4, H, D, device=dev).to(dt)
+            c2 = torch.randn(S4, H, D, device=dev).to(dt)
+            ms = timed(lambda: cpa.cp_lse_merge(c1, l1, c2, l2, out=c1, lse=l1), reps)
+            nbytes = 3 * c1.numel() * esz + 3 * l1.numel() * 4
+            out[f"lse_merge_{name}_s65536_h32_d128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                                       "bytes": nbytes}
+            del c1, c2
+        del l1, l2
         # Ulysses seq2head + head2seq at S=32768, H=32, D=128, P=16 (bf16)
         Su, Pu = 32768, 16
         x = torch.randn(Su, H, D, device=dev).to(torch.bfloat16)
@@ -273,6 +292,72 @@ def bench_ours(args):
         out["ulysses_seq2head_s32768_h32_d128_p16"] = {"ms": ms1, "gbs": nbytes / (ms1 * 1e-3) / 1e9, "bytes": nbytes}
         out["ulysses_head2seq_s32768_h32_d128_p16"] = {"ms": ms2, "gbs": nbytes / (ms2 * 1e-3) / 1e9, "bytes": nbytes}
         del x, y
+        return out
+
+    def ulysses_fwd(reps):
+        """Ulysses forward at S=32768, H=32, D=128, P=16 (2 heads per virtual rank):
+        the whole driver (seq2head of q, k, v; attention; head2seq of out) and its
+        four permutes on their own, device-resident inputs."""
+        Su, Pu = 32768, 16
+        qu, ku, vu = (t.to(dev) for t in make_inputs(Su, H, H, D, torch.bfloat16, 0))
+        ou, lu = torch.empty_like(qu), torch.empty(H, Su, dtype=torch.float32, device=dev)
+        wu = torch.empty(cpa.cp_workspace_size("ulysses_fwd", Su, H, H, D, torch.bfloat16, Pu),
+                         dtype=torch.uint8, device=dev)
+        y = [torch.empty(Pu, Su, H // Pu, D, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        total = timed(lambda: cpa.cp_ulysses_attention(qu, ku, vu, Pu, out=ou, lse=lu, workspace=wu), reps)
+
+        def perms():
+            for x, yy in zip((qu, ku, vu), y):
+                cpa.cp_ulysses_seq2head(x, Pu, y=yy)
+            cpa.cp_ulysses_head2seq(y[0], Pu, x=ou)
+
+        perm = timed(perms, reps)
+        f = causal_flop(Su, H, D)
+        nbytes = 4 * 2 * qu.numel() * 2
+        del qu, ku, vu, ou, lu, wu, y
+        return {"workload": "ulysses_fwd_s32768_h32_d128_bf16_p16", "flop": f, "driver_ms": total,
+                "driver_tflops": f / (total * 1e-3) / 1e12, "permute_ms": perm,
+                "permute_gbs": nbytes / (perm * 1e-3) / 1e9,
+                "attention_ms": total - perm, "attention_tflops": f / ((total - perm) * 1e-3) / 1e12}
+
+    def varlen_fwd(reps):
+        """Packed varlen ring forward at S=131072, Hq=32, Hkv=8, D=128, P=8, documents
+        of U[512, 16384] tokens (seed 0): attention phase on reordered inputs per
+        strategy; FLOP count only the visible (same-document, causal) pairs."""
+        from synth import cu_seqlens_from_lengths, doc_lengths
+
+        Sv, Hqv, Hkvv, Pv = 131072, 32, 8, 8
+        cu = cu_seqlens_from_lengths(doc_lengths(Sv, 512, 16384, seed=0))
+        lens = np.diff(cu).astype(np.int64)
+        pairs = float(np.sum(lens * (lens + 1) // 2))
+        f = 4.0 * D * Hqv * pairs
+        # visible pairs of each virtual rank's queries (every key of the sequence is visited)
+        pos = np.arange(Sv)
+        start = np.repeat(cu[:-1], lens)
+        vis = (pos - start + 1).astype(np.float64)
+        C = Sv // (2 * Pv)
+        out = {"workload": "packed_varlen_fwd_s131072_hq32_hkv8_d128_bf16_p8", "docs": int(len(lens)),
+               "flop": f, "visible_pairs_per_head": pairs}
+        qv, kv, vv = (t.to(dev) for t in make_inputs(Sv, Hqv, Hkvv, D, torch.bfloat16, 0))
+        cu_d = torch.from_numpy(cu).to(dev)
+        for layout in ("striped", "zigzag"):
+            if layout == "striped":
+                per_rank = [float(vis[r::Pv].sum()) for r in range(Pv)]
+                reo = lambda x: cpa.cp_striped_reorder(x, Pv)
+            else:
+                per_rank = [float(vis[r * C:(r + 1) * C].sum() + vis[(2 * Pv - 1 - r) * C:(2 * Pv - r) * C].sum())
+                            for r in range(Pv)]
+                reo = lambda x: cpa.cp_zigzag_reorder(x, Pv)
+            qr, kr, vr = reo(qv), reo(kv), reo(vv)
+            o = torch.empty_like(qr)
+            l = torch.empty(Hqv, Sv, dtype=torch.float32, device=dev)
+            ms = timed(lambda: cpa.cp_ring_attention_reordered(qr, kr, vr, Pv, layout, "fused", cu_seqlens=cu_d,
+                                                               out=o, lse=l), reps)
+            out[layout] = {"attention_ms": ms, "tflops": f / (ms * 1e-3) / 1e12,
+                           "rank_visible_pairs": per_rank,
+                           "imbalance_max_over_mean": max(per_rank) / (sum(per_rank) / Pv)}
+            del qr, kr, vr, o, l
+        del qv, kv, vv, cu_d
         return out
 
     def gqa_fwd_bwd(n_steps):
@@ -341,6 +426,8 @@ def bench_ours(args):
         torch.distributed.barrier()
     fb = gqa_fwd_bwd(args.fwd_bwd_steps) if args.fwd_bwd_steps > 0 else None
     hbm = hbm_parts(max(5, min(args.steps, 20)))
+    uly = ulysses_fwd(5) if args.fwd_bwd_steps > 0 else None
+    vlen = varlen_fwd(5) if args.fwd_bwd_steps > 0 else None
     sampler.mark_end()
     clocks = sampler.finish()
     st = cpa.cp_check_device_status()
@@ -418,6 +505,11 @@ def bench_ours(args):
                          "kernel": "attn_fwd_tc (ring, fused)", "peak_source": peaks["source"] + " burst bf16"},
             "fwd_bwd": None if fb is None else dict(fb, frac_of_peak=fb["fwd_bwd_tflops"] / peak),
             "hbm_kernels": {k: dict(v, frac_of_hbm=v["gbs"] / peaks["hbm_gbs"]) for k, v in hbm.items()},
+            "ulysses_fwd": None if uly is None else dict(
+                uly, frac_of_peak=uly["attention_tflops"] / peak,
+                permute_frac_of_hbm=uly["permute_gbs"] / peaks["hbm_gbs"]),
+            "varlen_fwd": None if vlen is None else dict(
+                vlen, frac_of_peak={k: vlen[k]["tflops"] / peak for k in ("striped", "zigzag")}),
             "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,
                       "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
                       "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},

@@ -7,14 +7,21 @@
 // without overflow; a row where both parts are empty (-inf) stays empty.
 //
 // HBM-bound: per row and head, 3*D elements of o move (two reads, one write)
-// and 3 lse floats.  One thread handles one 16-byte vector of o (4 fp32 or 8
-// bf16 elements); the D/elements-per-vector threads of one (row, head) are
-// lanes of one warp, so the lse of that row is read by all of them before any
-// of them writes it (in-place merge is allowed).
+// and 3 lse floats.  One block takes a tile of kRows consecutive rows and every
+// head: its threads first read the tile's lse values (kRows consecutive floats
+// per head, whole 32-byte sectors), form the weights into shared memory and
+// write the merged lse; then they stream the tile's o rows, which are one
+// contiguous range of kRows*H*D elements, four 16-byte vectors in flight per
+// thread (the first four issued before the weights are formed).  Each lse value and each o vector is read and written by the same
+// thread, so an in-place merge (o = o1, lse = lse1) is safe.
 #include "common.cuh"
 
 namespace cpa {
 namespace {
+
+constexpr int kRows = 8;       // rows per block
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;     // o vectors in flight per thread
 
 struct MergeParams {
   const void* o1;
@@ -23,9 +30,8 @@ struct MergeParams {
   const float* lse2;
   void* o;
   float* lse;
-  uint64_t total_vec;
   uint32_t Sq, H, D;
-  uint32_t vec_per_row;  // D / elements per vector
+  uint32_t vph;  // 16-byte vectors per (row, head): D / elements per vector
 };
 
 __device__ __forceinline__ void merge_weights(float l1, float l2, float* w1, float* w2,
@@ -44,52 +50,68 @@ __device__ __forceinline__ void merge_weights(float l1, float l2, float* w1, flo
 }
 
 template <bool kF32>
-__global__ void __launch_bounds__(256) lse_merge_kernel(MergeParams p) {
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  // Every lane of a warp runs the same number of iterations, so __syncwarp is safe.
-  const uint64_t warp_base = ((uint64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u));
-  const uint32_t lane = threadIdx.x & 31u;
-  for (uint64_t wb = warp_base; wb < p.total_vec; wb += stride) {
-    uint64_t v = wb + lane;
-    bool active = v < p.total_vec;
-    float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
-    uint32_t i = 0, h = 0;
-    bool head_lane = false;
-    if (active) {
-      uint64_t rh = v / p.vec_per_row;  // row*H + head
-      head_lane = (v - rh * p.vec_per_row) == 0;
-      i = (uint32_t)(rh / p.H);
-      h = (uint32_t)(rh - (uint64_t)i * p.H);
-      uint64_t li = (uint64_t)h * p.Sq + i;
-      merge_weights(p.lse1[li], p.lse2[li], &w1, &w2, &lnew);
-    }
-    __syncwarp();
-    if (active) {
-      if (kF32) {
-        float4 a = reinterpret_cast<const float4*>(p.o1)[v];
-        float4 b = reinterpret_cast<const float4*>(p.o2)[v];
-        float4 r;
-        r.x = a.x * w1 + b.x * w2;
-        r.y = a.y * w1 + b.y * w2;
-        r.z = a.z * w1 + b.z * w2;
-        r.w = a.w * w1 + b.w * w2;
-        reinterpret_cast<float4*>(p.o)[v] = r;
-      } else {
-        uint4 a = reinterpret_cast<const uint4*>(p.o1)[v];
-        uint4 b = reinterpret_cast<const uint4*>(p.o2)[v];
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-        uint4 r;
-        __nv_bfloat162* r2 = reinterpret_cast<__nv_bfloat162*>(&r);
+__device__ __forceinline__ uint4 merge_vec(uint4 a, uint4 b, float2 w) {
+  uint4 r;
+  if (kF32) {
+    r.x = __float_as_uint(__uint_as_float(a.x) * w.x + __uint_as_float(b.x) * w.y);
+    r.y = __float_as_uint(__uint_as_float(a.y) * w.x + __uint_as_float(b.y) * w.y);
+    r.z = __float_as_uint(__uint_as_float(a.z) * w.x + __uint_as_float(b.z) * w.y);
+    r.w = __float_as_uint(__uint_as_float(a.w) * w.x + __uint_as_float(b.w) * w.y);
+  } else {
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    __nv_bfloat162* r2 = reinterpret_cast<__nv_bfloat162*>(&r);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float2 fa = __bfloat1622float2(a2[k]);
-          float2 fb = __bfloat1622float2(b2[k]);
-          r2[k] = __floats2bfloat162_rn(fa.x * w1 + fb.x * w2, fa.y * w1 + fb.y * w2);
-        }
-        reinterpret_cast<uint4*>(p.o)[v] = r;
+    for (int k = 0; k < 4; ++k) {
+      float2 fa = __bfloat1622float2(a2[k]);
+      float2 fb = __bfloat1622float2(b2[k]);
+      r2[k] = __floats2bfloat162_rn(fa.x * w.x + fb.x * w.y, fa.y * w.x + fb.y * w.y);
+    }
+  }
+  return r;
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(MergeParams p) {
+  extern __shared__ float2 w_sm[];  // [kRows][H] (w1, w2)
+  const uint32_t i0 = blockIdx.x * kRows;
+  const uint32_t rows = min((uint32_t)kRows, p.Sq - i0);
+  // the tile's o rows: one contiguous range of vectors
+  const uint64_t base = (uint64_t)i0 * p.H * p.vph;
+  const uint32_t n = rows * p.H * p.vph;
+  const uint4* a = reinterpret_cast<const uint4*>(p.o1) + base;
+  const uint4* b = reinterpret_cast<const uint4*>(p.o2) + base;
+  uint4* o = reinterpret_cast<uint4*>(p.o) + base;
+  uint4 va[kUnroll], vb[kUnroll];
+  auto load = [&](uint32_t v0) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t v = v0 + u * kThreads;
+      if (v < n) {
+        va[u] = __ldcs(a + v);
+        vb[u] = __ldcs(b + v);
       }
-      if (head_lane) p.lse[(uint64_t)h * p.Sq + i] = lnew;
+    }
+  };
+  load(threadIdx.x);  // the first vectors are in flight while the weights are formed
+  // weights and merged lse of the tile: thread t takes (head t / kRows, row t % kRows)
+  for (uint32_t t = threadIdx.x; t < (uint32_t)kRows * p.H; t += kThreads) {
+    const uint32_t h = t / kRows, r = t - h * kRows;
+    if (r < rows) {
+      const uint64_t li = (uint64_t)h * p.Sq + i0 + r;
+      float w1, w2, lnew;
+      merge_weights(p.lse1[li], p.lse2[li], &w1, &w2, &lnew);
+      w_sm[r * p.H + h] = make_float2(w1, w2);
+      p.lse[li] = lnew;
+    }
+  }
+  __syncthreads();
+  for (uint32_t v0 = threadIdx.x; v0 < n; v0 += kThreads * kUnroll) {
+    if (v0 != threadIdx.x) load(v0);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t v = v0 + u * kThreads;
+      if (v < n) __stcs(o + v, merge_vec<kF32>(va[u], vb[u], w_sm[v / p.vph]));
     }
   }
 }
@@ -110,15 +132,25 @@ cp_status launch_lse_merge(const void* o1, const float* lse1, const void* o2, co
   p.Sq = (uint32_t)Sq;
   p.H = (uint32_t)H;
   p.D = (uint32_t)D;
-  uint32_t epv = o_f32 ? 4 : 8;
-  p.vec_per_row = (uint32_t)D / epv;
-  p.total_vec = (uint64_t)Sq * H * p.vec_per_row;
-  uint64_t want = (p.total_vec + 255) / 256;
-  uint32_t blocks = (uint32_t)(want < 152ull * 32 ? want : 152ull * 32);
+  p.vph = (uint32_t)D / (o_f32 ? 4u : 8u);  // a row of one head is a whole number of vectors
+  if ((uint64_t)kRows * H * p.vph > 0xffffffffull || (uint64_t)Sq > 0xffffffffull) {
+    set_last_error("lse merge: too many rows or heads for one launch");
+    return CP_ERR_UNSUPPORTED;
+  }
+  const size_t smem = (size_t)kRows * H * sizeof(float2);
+  if (smem > 48 * 1024) {
+    set_last_error("lse merge: too many heads for one block's weight table");
+    return CP_ERR_UNSUPPORTED;
+  }
+  const uint64_t blocks = ((uint64_t)Sq + kRows - 1) / kRows;
+  if (blocks > 0x7fffffffull) {
+    set_last_error("lse merge: too many rows for one launch");
+    return CP_ERR_UNSUPPORTED;
+  }
   if (o_f32)
-    lse_merge_kernel<true><<<blocks, 256, 0, st>>>(p);
+    lse_merge_kernel<true><<<(unsigned)blocks, kThreads, smem, st>>>(p);
   else
-    lse_merge_kernel<false><<<blocks, 256, 0, st>>>(p);
+    lse_merge_kernel<false><<<(unsigned)blocks, kThreads, smem, st>>>(p);
   return cuda_check(cudaGetLastError(), "lse_merge_kernel launch");
 }
 

@@ -69,7 +69,7 @@ def test_ulysses_permute_bitexact(dtype, S, H, D, P):
 # ---------------------------------------------------------------- LSE merge
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
-@pytest.mark.parametrize("Sq,H,D", [(1, 1, 64), (333, 8, 128), (4096, 32, 128)])
+@pytest.mark.parametrize("Sq,H,D", [(1, 1, 64), (333, 8, 128), (4096, 32, 128), (77, 3, 48), (50, 96, 32)])
 def test_lse_merge(dtype, Sq, H, D):
     g = torch.Generator().manual_seed(21)
     o1 = torch.randn(Sq, H, D, generator=g).to(dtype)
