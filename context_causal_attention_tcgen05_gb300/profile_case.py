@@ -5,7 +5,8 @@
 
 Cases: ring_fwd (reordered inputs, fused ring: one attention launch per rep),
 ring_bwd (ring backward; one tcgen05 backward launch per rep), permute
-(zigzag reorder of q), ulysses (seq2head of q).  Inputs are N(0,1) bf16 from
+(zigzag reorder of q), ulysses (seq2head of q), merge (in-place fp32 LSE
+merge of two [S, Hq, D] partial outputs).  Inputs are N(0,1) bf16 from
 the shared seeded generators.  Exits non-zero if the library reports an error.
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ import context_causal_attention_tcgen05_gb300 as cpa
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["ring_fwd", "ring_bwd", "permute", "ulysses"], required=True)
+    ap.add_argument("--case", choices=["ring_fwd", "ring_bwd", "permute", "ulysses", "merge"], required=True)
     ap.add_argument("--S", type=int, default=8192)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)
@@ -48,6 +49,14 @@ def main(argv=None) -> int:
                          dtype=torch.uint8, device=q.device)
         for _ in range(a.reps):
             cpa.cp_ring_attention_bwd(q, k, v, o, l, do, a.P, a.layout, workspace=ws)
+    elif a.case == "merge":
+        g = torch.Generator(device="cuda").manual_seed(1)
+        o1 = torch.randn(a.S, a.Hq, a.D, device="cuda", generator=g)
+        o2 = torch.randn(a.S, a.Hq, a.D, device="cuda", generator=g)
+        l1 = torch.randn(a.Hq, a.S, device="cuda", generator=g)
+        l2 = torch.randn(a.Hq, a.S, device="cuda", generator=g)
+        for _ in range(a.reps):
+            cpa.cp_lse_merge(o1, l1, o2, l2, out=o1, lse=l1)
     elif a.case == "permute":
         y = torch.empty_like(q)
         for _ in range(a.reps):
