@@ -106,6 +106,9 @@ FWD_CASES = [
     (64, 64, 2, 2, 64, 1, 3, 4, 4, None),             # striped rank 1 vs rank 3 (first row empty)
     (256, 256, 4, 2, 128, 0, 0, 1, 1, [50, 1, 77, 128]),   # packed documents
     (20, 30, 2, 2, 64, 0, 25, 1, 1, None),            # every row fully masked
+    # 640 units of two query tiles for 148+ CTAs: each CTA walks several, alternating a
+    # unit whose rows see no key (rows < 300) and a unit with a single query tile
+    (356, 200, 320, 32, 128, 0, 300, 1, 1, None),
 ]
 
 
