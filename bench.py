@@ -450,35 +450,78 @@ def bench_ours(args):
     perm_bytes = 3 * 2 * tensor_bytes + 2 * tensor_bytes + 2 * S * H * 4
     perm_gbs = perm_bytes / (statistics.mean(perm_ms) * 1e-3) / 1e9
 
-    # end to end through the public one-call driver with host buffers
+    # end to end through the public one-call driver with host buffers: every step
+    # copies its q, k, v from pinned host memory and reads out and lse back.  Steps
+    # are independent, so they are pipelined as a user would run them: two device
+    # buffer sets, copy-in / compute / copy-out on three streams (step i's copy-in
+    # overlaps step i-1's compute and step i-2's copy-out).  The inputs of a step
+    # (192 MiB) exceed L2, so no flush is needed between steps.
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
-    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_p = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     wsz = cpa.cp_workspace_size("ring_fwd", S, H, H, D, torch.bfloat16, P, "fused")
-    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = 2
+    bufs = [dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v), o=torch.empty_like(q),
+                 l=torch.empty_like(lse), w=torch.empty(wsz, dtype=torch.uint8, device=dev),
+                 op=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                 lp=torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for _ in range(nb)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = [dict(inp=torch.cuda.Event(), cmp=torch.cuda.Event(), out=torch.cuda.Event()) for _ in range(nb)]
 
-    def e2e_step():
-        qd.copy_(q_p, non_blocking=True)
-        kd.copy_(k_p, non_blocking=True)
-        vd.copy_(v_p, non_blocking=True)
-        cpa.cp_ring_attention(qd, kd, vd, P, layout, "fused", out=out, lse=lse, workspace=work)
-        out_p.copy_(out, non_blocking=True)
-        lse_p.copy_(lse, non_blocking=True)
+    def e2e_run(n_steps, start_ev=None, end_ev=None):
+        torch.cuda.synchronize()
+        if start_ev is not None:
+            start_ev.record(s_in)
+            s_cmp.wait_stream(s_in)
+            s_out.wait_stream(s_in)
+        for i in range(n_steps):
+            bb, e = bufs[i % nb], ev[i % nb]
+            if i >= nb:
+                s_in.wait_event(e["cmp"])  # the compute that read this buffer set is done
+            with torch.cuda.stream(s_in):
+                bb["q"].copy_(q_p, non_blocking=True)
+                bb["k"].copy_(k_p, non_blocking=True)
+                bb["v"].copy_(v_p, non_blocking=True)
+            e["inp"].record(s_in)
+            s_cmp.wait_event(e["inp"])
+            if i >= nb:
+                s_cmp.wait_event(e["out"])  # the copy-out of this buffer set's last result is done
+            cpa.cp_ring_attention(bb["q"], bb["k"], bb["v"], P, layout, "fused", out=bb["o"], lse=bb["l"],
+                                  workspace=bb["w"], stream=s_cmp)
+            e["cmp"].record(s_cmp)
+            s_out.wait_event(e["cmp"])
+            with torch.cuda.stream(s_out):
+                bb["op"].copy_(bb["o"], non_blocking=True)
+                bb["lp"].copy_(bb["l"], non_blocking=True)
+            e["out"].record(s_out)
+        if end_ev is not None:
+            s_out.wait_stream(s_in)
+            s_out.wait_stream(s_cmp)
+            end_ev.record(s_out)
+        torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
+    e2e_run(max(3, args.warmup))
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_run(args.steps, ea, eb)
+    e2e_mean = ea.elapsed_time(eb) / args.steps
+    # the same step without overlap (one stream, one step at a time), for reference
+    ser = []
+    for i in range(min(args.steps, 20)):
+        bb = bufs[0]
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        bb["q"].copy_(q_p, non_blocking=True)
+        bb["k"].copy_(k_p, non_blocking=True)
+        bb["v"].copy_(v_p, non_blocking=True)
+        cpa.cp_ring_attention(bb["q"], bb["k"], bb["v"], P, layout, "fused", out=bb["o"], lse=bb["l"],
+                              workspace=bb["w"])
+        bb["op"].copy_(bb["o"], non_blocking=True)
+        bb["lp"].copy_(bb["l"], non_blocking=True)
+        b_.record(stream)
+        ser.append((a_, b_))
     torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.fill_(1.0)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        e2e_ms.append((a, b))
-    torch.cuda.synchronize()
-    e2e_mean = statistics.mean(a.elapsed_time(b) for a, b in e2e_ms)
+    e2e_serial = statistics.mean(x.elapsed_time(y) for x, y in ser)
+    st = cpa.cp_check_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {cpa.cp_last_error()}")
     if ws > 1:
         t = torch.tensor([e2e_mean], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -514,7 +557,10 @@ def bench_ours(args):
                       "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
                       "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * tensor_bytes,
-                    "d2h_bytes_per_step": tensor_bytes + S * H * 4, "ms_per_step": e2e_mean},
+                    "d2h_bytes_per_step": tensor_bytes + S * H * 4, "ms_per_step": e2e_mean,
+                    "pipeline": "2 buffer sets; copy-in, compute, copy-out on 3 streams",
+                    "serial_ms_per_step": e2e_serial,
+                    "serial_value": flop / (e2e_serial * 1e-3) / 1e12},
             "clocks": clocks,
         }
         if cpu_tf is not None:
