@@ -434,15 +434,18 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
       const float* lse_st = lse_all + st * 2 * kTileRows + cb;
       const float* del_st = lse_st + kTileRows;
-      // phase 1: P^T = 2^(S^T*scale*log2e - lse*log2e), 32 columns at a time
+      // phase 1: P^T = 2^(S^T*scale*log2e - lse*log2e)
       if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
       float p[64];
+      uint32_t sr2[2][32];  // both halves in flight before one wait
+      ptx::tmem_ld32(lane_addr + cb, sr2[0]);
+      ptx::tmem_ld32(lane_addr + cb + 32, sr2[1]);
+      ptx::tmem_wait_ld_regs(sr2[0]);
+      ptx::tmem_wait_ld_regs(sr2[1]);
 #pragma unroll
       for (int hc = 0; hc < 64; hc += 32) {
-        uint32_t sr[32];
-        ptx::tmem_ld32(lane_addr + cb + hc, sr);
-        ptx::tmem_wait_ld_regs(sr);
+        const uint32_t* sr = sr2[hc / 32];
         if (t.full) {  // every pair visible: no per-column mask
 #pragma unroll
           for (int cc = 0; cc < 32; cc += 4) {
@@ -857,16 +860,19 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         }
       }
       const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
-      // phase 1: P from S (32 columns at a time), then release S for the next tile
+      // phase 1: P from S, then release S for the next tile
       if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
       float p[64];
       const bool fast = t.full && nq_tile == kTileRows;  // every pair visible: no per-column mask
+      uint32_t sr2[2][32];  // both halves in flight before one wait
+      ptx::tmem_ld32(lane_addr + cb, sr2[0]);
+      ptx::tmem_ld32(lane_addr + cb + 32, sr2[1]);
+      ptx::tmem_wait_ld_regs(sr2[0]);
+      ptx::tmem_wait_ld_regs(sr2[1]);
 #pragma unroll
       for (int hc = 0; hc < 64; hc += 32) {
-        uint32_t sr[32];
-        ptx::tmem_ld32(lane_addr + cb + hc, sr);
-        ptx::tmem_wait_ld_regs(sr);
+        const uint32_t* sr = sr2[hc / 32];
         if (fast) {
 #pragma unroll
           for (int cc = 0; cc < 32; cc += 2) {
