@@ -19,7 +19,9 @@ from .context import (
     ring_attention,
     seq_to_head,
     ulysses_attention,
+    ulysses_attention_bwd,
     ulysses_head2seq,
+    ulysses_kv_replicas,
     ulysses_seq2head,
     work,
 )
@@ -27,5 +29,6 @@ from .context import (
 __all__ = [
     "attention", "attention_bwd", "doc_index", "positions", "visible_mask", "visible_pairs",
     "head_to_seq", "lse_merge", "rank_positions", "rank_visible_pairs", "reorder", "restore",
-    "ring_attention", "seq_to_head", "ulysses_attention", "ulysses_head2seq", "ulysses_seq2head", "work",
+    "ring_attention", "seq_to_head", "ulysses_attention", "ulysses_attention_bwd", "ulysses_head2seq",
+    "ulysses_kv_replicas", "ulysses_seq2head", "work",
 ]

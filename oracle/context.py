@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .block_attention import attention, visible_pairs
+from .block_attention import attention, attention_bwd, visible_pairs
 
 __all__ = [
     "lse_merge",
@@ -41,6 +41,8 @@ __all__ = [
     "restore",
     "ring_attention",
     "ulysses_attention",
+    "ulysses_attention_bwd",
+    "ulysses_kv_replicas",
     "work",
     "rank_visible_pairs",
 ]
@@ -189,20 +191,44 @@ def ring_attention(q, k, v, P: int, layout: str = "contiguous", causal: bool = T
     return out, lse, counts
 
 
+def ulysses_kv_replicas(Hq: int, Hkv: int, P: int) -> int:
+    """Copies of each key/value head in the Ulysses exchange.
+
+    The exchange gives every rank H/P heads, so with fewer key/value heads than
+    ranks the key/value heads are replicated first ("replicating the KV by
+    group", the handbook's note on grouped-query attention under Ulysses):
+    each head is repeated R = P / Hkv times, consecutive copies, so that rank p
+    receives copy p of the repeated heads, which is original head p // R -- the
+    head its query heads p*Hq/P ... read under the consecutive grouping.  R = 1
+    when Hkv % P == 0 (no replication)."""
+    assert Hq % P == 0, "Ulysses degree is limited by the query heads"
+    if Hkv % P == 0:
+        return 1
+    assert P % Hkv == 0, "replication needs P to be a multiple of the key/value heads"
+    return P // Hkv
+
+
+def _ulysses_inputs(q, k, v, P: int):
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    R = ulysses_kv_replicas(q.shape[1], k.shape[1], P)
+    if R > 1:
+        k = np.repeat(k, R, axis=1)
+        v = np.repeat(v, R, axis=1)
+    return q, k, v, R
+
+
 def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None):
     """The Ulysses scheme over P virtual ranks, restated from the Ulysses section.
 
     Each rank's slice of q, k, v goes through ``seq_to_head``; rank p runs
     full-sequence attention over its H/P query heads (and Hkv/P key/value
-    heads); ``head_to_seq`` brings the output back.  Returns (out [S, Hq, D],
-    lse [Hq, S]).
+    heads, or the one replicated head, ``ulysses_kv_replicas``);
+    ``head_to_seq`` brings the output back.  Returns (out [S, Hq, D], lse [Hq, S]).
     """
-    q = np.asarray(q, dtype=np.float64)
-    k = np.asarray(k, dtype=np.float64)
-    v = np.asarray(v, dtype=np.float64)
-    S, Hq, D = q.shape
-    Hkv = k.shape[1]
-    assert Hq % P == 0 and Hkv % P == 0, "Ulysses degree is limited by the head counts"
+    q, k, v, _ = _ulysses_inputs(q, k, v, P)
+    S = q.shape[0]
     C = S // P
     sl = [slice(r * C, (r + 1) * C) for r in range(P)]
     qh = seq_to_head([q[s] for s in sl], P)
@@ -216,6 +242,37 @@ def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None):
     out = np.concatenate(head_to_seq(outs, P), axis=0)
     lse = np.concatenate(lses, axis=0)  # rank p holds query heads [p*Hq/P, (p+1)*Hq/P)
     return out, lse
+
+
+def ulysses_attention_bwd(q, k, v, dout, P: int, causal: bool = True, cu_seqlens=None):
+    """Backward of the Ulysses scheme, restated rank by rank.
+
+    head_to_seq is the backward of seq_to_head (a permutation), so the gradients
+    travel the same exchange as the outputs: q, k, v and dout go through
+    ``seq_to_head``; rank p takes the exact gradient of its full-sequence
+    attention; ``head_to_seq`` brings dq, dk, dv back.  Replicated key/value
+    heads (``ulysses_kv_replicas``) sum their copies' gradients.  Returns
+    (dq [S, Hq, D], dk [S, Hkv, D], dv [S, Hkv, D])."""
+    Hkv = np.asarray(k).shape[1]
+    q, k, v, R = _ulysses_inputs(q, k, v, P)
+    dout = np.asarray(dout, dtype=np.float64)
+    S = q.shape[0]
+    C = S // P
+    sl = [slice(r * C, (r + 1) * C) for r in range(P)]
+    qh, kh, vh, doh = (seq_to_head([x[s] for s in sl], P) for x in (q, k, v, dout))
+    dqs, dks, dvs = [], [], []
+    for p in range(P):
+        dq_p, dk_p, dv_p = attention_bwd(qh[p], kh[p], vh[p], doh[p], causal, cu_seqlens=cu_seqlens)
+        dqs.append(dq_p)
+        dks.append(dk_p)
+        dvs.append(dv_p)
+    dq = np.concatenate(head_to_seq(dqs, P), axis=0)
+    dk = np.concatenate(head_to_seq(dks, P), axis=0)
+    dv = np.concatenate(head_to_seq(dvs, P), axis=0)
+    if R > 1:  # the copies of a head are consecutive
+        dk = dk.reshape(S, Hkv, R, -1).sum(axis=2)
+        dv = dv.reshape(S, Hkv, R, -1).sum(axis=2)
+    return dq, dk, dv
 
 
 def work(query_chunks):

@@ -352,6 +352,39 @@ def test_ulysses_restatement_equals_unpartitioned(Hq, Hkv, P):
     assert np.abs(o - ref_o).max() < 1e-12 and np.abs(l - ref_l).max() < 1e-12
 
 
+@pytest.mark.parametrize("Hq,Hkv,P", [(8, 2, 4), (8, 1, 8), (4, 2, 4)])
+def test_ulysses_replicated_kv_equals_unpartitioned(Hq, Hkv, P):
+    # fewer key/value heads than ranks: each head is copied P/Hkv times before the exchange
+    S, D = 24, 8
+    q, k, v = _rand((S, Hq, D), 113), _rand((S, Hkv, D), 114), _rand((S, Hkv, D), 115)
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = oracle.ulysses_attention(q, k, v, P)
+    assert np.abs(o - ref_o).max() < 1e-12 and np.abs(l - ref_l).max() < 1e-12
+
+
+@pytest.mark.parametrize("Hq,Hkv,P,docs", [(8, 8, 4, None), (8, 4, 2, None), (8, 2, 4, None), (8, 1, 8, None),
+                                           (4, 4, 2, [5, 11, 8])])
+def test_ulysses_bwd_restatement_equals_unpartitioned(Hq, Hkv, P, docs):
+    # the rank-by-rank Ulysses backward (replicated heads summed) is the plain gradient
+    S, D = 24, 8
+    q, k, v = _rand((S, Hq, D), 116), _rand((S, Hkv, D), 117), _rand((S, Hkv, D), 118)
+    do = _rand((S, Hq, D), 119)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu)
+    dq, dk, dv = oracle.ulysses_attention_bwd(q, k, v, do, P, cu_seqlens=cu)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert got.shape == ref.shape
+        assert np.abs(got - ref).max() < 1e-12
+
+
+def test_ulysses_kv_replicas_counts():
+    assert oracle.ulysses_kv_replicas(32, 8, 4) == 1
+    assert oracle.ulysses_kv_replicas(32, 8, 16) == 2
+    assert oracle.ulysses_kv_replicas(32, 1, 32) == 32
+    with pytest.raises(AssertionError):
+        oracle.ulysses_kv_replicas(32, 8, 12)  # 12 is neither a divisor nor a multiple of 8
+
+
 def test_tiny_exact_workload_both_schemes():
     # The handbook's own data: S=32, H=8, D=16, P=4, ring and Ulysses vs unpartitioned.
     q, k, v = (t.double().numpy() for t in make_qkv())
