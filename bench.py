@@ -314,11 +314,20 @@ def bench_ours(args):
         perm = timed(perms, reps)
         f = causal_flop(Su, H, D)
         nbytes = 4 * 2 * qu.numel() * 2
-        del qu, ku, vu, ou, lu, wu, y
+        # backward through the public driver (dO ~ N(0,1), seed 1)
+        dou = torch.randn(qu.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+        wb = torch.empty(cpa.cp_workspace_size("ulysses_bwd", Su, H, H, D, torch.bfloat16, Pu),
+                         dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(qu), torch.empty_like(ku), torch.empty_like(vu)
+        bwd = timed(lambda: cpa.cp_ulysses_attention_bwd(qu, ku, vu, ou, lu, dou, Pu, dq=dq, dk=dk, dv=dv,
+                                                         workspace=wb), reps)
+        del qu, ku, vu, ou, lu, wu, y, dou, wb, dq, dk, dv
         return {"workload": "ulysses_fwd_s32768_h32_d128_bf16_p16", "flop": f, "driver_ms": total,
                 "driver_tflops": f / (total * 1e-3) / 1e12, "permute_ms": perm,
                 "permute_gbs": nbytes / (perm * 1e-3) / 1e9,
-                "attention_ms": total - perm, "attention_tflops": f / ((total - perm) * 1e-3) / 1e12}
+                "attention_ms": total - perm, "attention_tflops": f / ((total - perm) * 1e-3) / 1e12,
+                "bwd_driver_ms": bwd, "bwd_tflops": 2.5 * f / (bwd * 1e-3) / 1e12,
+                "fwd_bwd_tflops": 3.5 * f / ((total + bwd) * 1e-3) / 1e12}
 
     def varlen_fwd(reps):
         """Packed varlen ring forward at S=131072, Hq=32, Hkv=8, D=128, P=8, documents
@@ -550,7 +559,8 @@ def bench_ours(args):
             "hbm_kernels": {k: dict(v, frac_of_hbm=v["gbs"] / peaks["hbm_gbs"]) for k, v in hbm.items()},
             "ulysses_fwd": None if uly is None else dict(
                 uly, frac_of_peak=uly["attention_tflops"] / peak,
-                permute_frac_of_hbm=uly["permute_gbs"] / peaks["hbm_gbs"]),
+                permute_frac_of_hbm=uly["permute_gbs"] / peaks["hbm_gbs"],
+                fwd_bwd_frac_of_peak=uly["fwd_bwd_tflops"] / peak),
             "varlen_fwd": None if vlen is None else dict(
                 vlen, frac_of_peak={k: vlen[k]["tflops"] / peak for k in ("striped", "zigzag")}),
             "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,

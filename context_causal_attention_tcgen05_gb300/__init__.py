@@ -25,6 +25,7 @@ __all__ = [
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
     "cp_lse_reorder",
     "cp_ring_attention", "cp_ring_attention_reordered", "cp_ring_attention_bwd", "cp_ulysses_attention",
+    "cp_ulysses_attention_bwd",
     "cp_workspace_size", "cp_check_device_status", "cp_debug_bounded_wait",
     "cp_status_string", "cp_last_error", "cp_version",
     "CP_F32", "CP_BF16", "REORDER", "RING_MODE", "OP",
@@ -35,7 +36,8 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 CP_F32, CP_BF16 = 0, 1
 REORDER = {"contiguous": 0, "dual_chunk_swap": 1, "zigzag": 1, "striped": 2, "auto": 3}
 RING_MODE = {"fused": 0, "stepwise": 1}
-OP = {"ring_fwd": 0, "ring_bwd": 1, "ulysses_fwd": 2, "block_bwd": 3, "ring_fwd_reordered": 4}
+OP = {"ring_fwd": 0, "ring_bwd": 1, "ulysses_fwd": 2, "block_bwd": 3, "ring_fwd_reordered": 4,
+      "ulysses_bwd": 5}
 
 _c_i32, _c_i64, _c_f32, _c_p, _c_size = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
@@ -68,6 +70,8 @@ _SIGS = {
                               _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ulysses_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p,
                              _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
+    "cp_ulysses_attention_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32,
+                                 _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_workspace_size": [_c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                           ctypes.POINTER(_c_size)],
     "cp_check_device_status": [_c_p],
@@ -363,6 +367,24 @@ def cp_ulysses_attention(q, k, v, P, cu_seqlens=None, out=None, lse=None, worksp
         _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P, _ptr(cu_seqlens), n_docs, _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
+
+
+def cp_ulysses_attention_bwd(q, k, v, out, lse, dout, P, cu_seqlens=None, dq=None, dk=None, dv=None,
+                             workspace=None, stream=None):
+    """Backward of cp_ulysses_attention: (dq, dk, dv) from the forward's out and lse."""
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = _workspace(cp_workspace_size("ulysses_bwd", S, Hq, Hkv, D, q.dtype, P), q.device)
+    n_docs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check("cp_ulysses_attention_bwd", load_library().cp_ulysses_attention_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), S, Hq, Hkv, D, _dt(q), P,
+        _ptr(cu_seqlens), n_docs, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return dq, dk, dv
 
 
 def cp_check_device_status(stream=None) -> int:

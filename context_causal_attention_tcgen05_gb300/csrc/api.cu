@@ -348,17 +348,53 @@ BlockBwdWs block_bwd_ws(int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t
   return w;
 }
 
+// Copies of each key/value head in the Ulysses exchange ("Ulysses: transposing
+// between the sequence and the heads": the exchange hands every rank H/P heads;
+// with fewer key/value heads than ranks they are replicated by group first).
+// R = 1 when Hkv % P == 0; R = P / Hkv when P % Hkv == 0; 0 (unsupported) otherwise.
+int32_t ulysses_kv_replicas(int32_t Hkv, int32_t P) {
+  if (Hkv % P == 0) return 1;
+  if (P % Hkv == 0) return P / Hkv;
+  return 0;
+}
+
 struct UlyssesWs {
   size_t q, k, v, o, total;
 };
-UlyssesWs ulysses_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype) {
+UlyssesWs ulysses_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P) {
   UlyssesWs w;
   size_t es = dtype_size(dtype);
+  const int32_t R = ulysses_kv_replicas(Hkv, P) > 0 ? ulysses_kv_replicas(Hkv, P) : 1;
   size_t off = 0;
   w.q = off; off += align_up((size_t)S * Hq * D * es);
-  w.k = off; off += align_up((size_t)S * Hkv * D * es);
-  w.v = off; off += align_up((size_t)S * Hkv * D * es);
+  w.k = off; off += align_up((size_t)S * Hkv * R * D * es);
+  w.v = off; off += align_up((size_t)S * Hkv * R * D * es);
   w.o = off; off += align_up((size_t)S * Hq * D * es);
+  w.total = off;
+  return w;
+}
+
+// Ulysses backward: q, k, v, dout in the head-major layout, lse and Delta in the
+// head-major row order, fp32 gradient accumulators in the head-major layout.
+struct UlyssesBwdWs {
+  size_t q, k, v, dout, delta, lse_h, delta_h, dq, dk, dv, total;
+};
+UlyssesBwdWs ulysses_bwd_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P) {
+  UlyssesBwdWs w;
+  size_t es = dtype_size(dtype);
+  const int32_t R = ulysses_kv_replicas(Hkv, P) > 0 ? ulysses_kv_replicas(Hkv, P) : 1;
+  const size_t nq = (size_t)S * Hq * D, nkv = (size_t)S * Hkv * R * D;
+  size_t off = 0;
+  w.q = off; off += align_up(nq * es);
+  w.k = off; off += align_up(nkv * es);
+  w.v = off; off += align_up(nkv * es);
+  w.dout = off; off += align_up(nq * es);
+  w.delta = off; off += align_up((size_t)S * Hq * 4);
+  w.lse_h = off; off += align_up((size_t)S * Hq * 4);
+  w.delta_h = off; off += align_up((size_t)S * Hq * 4);
+  w.dq = off; off += align_up(nq * 4);
+  w.dk = off; off += align_up(nkv * 4);
+  w.dv = off; off += align_up(nkv * 4);
   w.total = off;
   return w;
 }
@@ -654,7 +690,10 @@ cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hkv, int3
       *bytes = ring_bwd_ws(S, Hq, Hkv, D, dtype).total;
       return CP_OK;
     case CP_OP_ULYSSES_FWD:
-      *bytes = ulysses_ws(S, Hq, Hkv, D, dtype).total;
+      *bytes = ulysses_ws(S, Hq, Hkv, D, dtype, P).total;
+      return CP_OK;
+    case CP_OP_ULYSSES_BWD:
+      *bytes = ulysses_bwd_ws(S, Hq, Hkv, D, dtype, P).total;
       return CP_OK;
     case CP_OP_BLOCK_BWD:  // S is max(Sq, Sk) here
       *bytes = block_bwd_ws(S, S, Hq, Hkv, D).total;
@@ -839,17 +878,19 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   CP_TRY(check_common(Hq, Hkv, D, dtype));
   CP_REQUIRE(P >= 1 && P <= 64, CP_ERR_INVALID_ARG, "P must be in [1, 64]");
   CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
-  CP_REQUIRE(Hq % P == 0 && Hkv % P == 0, CP_ERR_SHAPE,
-             "Ulysses needs Hq % P == 0 and Hkv % P == 0 (degree limited by the key/value heads)");
+  CP_REQUIRE(Hq % P == 0, CP_ERR_SHAPE, "Ulysses needs Hq % P == 0");
+  CP_REQUIRE(ulysses_kv_replicas(Hkv, P) > 0, CP_ERR_SHAPE,
+             "Ulysses needs Hkv % P == 0, or P % Hkv == 0 (key/value heads replicated P/Hkv times)");
   CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "Ulysses needs S % P == 0");
   CP_REQUIRE(S * (int64_t)Hq < (int64_t)INT32_MAX && S * (int64_t)P < (int64_t)INT32_MAX,
              CP_ERR_UNSUPPORTED, "S*Hq and S*P must be < 2^31");
   CP_REQUIRE(!cu_seqlens || n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
   const size_t es = dtype_size(dtype);
-  CP_REQUIRE(((size_t)(Hkv / P) * D * es) % 16 == 0, CP_ERR_ALIGN,
+  const int32_t R = ulysses_kv_replicas(Hkv, P);
+  CP_REQUIRE(((size_t)(Hkv * R / P) * D * es) % 16 == 0, CP_ERR_ALIGN,
              "(Hkv/P)*D*sizeof(dtype) must be a multiple of 16 bytes");
   if (S == 0) return CP_OK;
-  UlyssesWs w = ulysses_ws(S, Hq, Hkv, D, dtype);
+  UlyssesWs w = ulysses_ws(S, Hq, Hkv, D, dtype, P);
   CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for Ulysses");
   CP_CHECK_T(workspace, "workspace", false);
   CP_CHECK_T(q, "q", false);
@@ -863,9 +904,14 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   void* vh = ws_at(workspace, w.v);
   void* oh = ws_at(workspace, w.o);
   CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
-  CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
-  CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
-  const int32_t Hqp = Hq / P, Hkvp = Hkv / P;
+  if (R == 1) {
+    CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  } else {  // rank p gets a copy of key/value head p / R
+    CP_TRY(launch_kv_replicate(k, kh, S, Hkv, (int64_t)D * es, P, st));
+    CP_TRY(launch_kv_replicate(v, vh, S, Hkv, (int64_t)D * es, P, st));
+  }
+  const int32_t Hqp = Hq / P, Hkvp = Hkv * R / P;
   Schedule* s = new Schedule;
   s->n_groups = 0;
   s->n_segs = 0;
@@ -881,6 +927,95 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   delete s;
   CP_TRY(stt);
   CP_TRY(launch_row_gather(kHead2Seq, oh, out, S, (int64_t)Hq * D * es, P, Hq, st));
+  return CP_OK;
+}
+
+cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, const void* out,
+                                   const float* lse, const void* dout, int64_t S, int32_t Hq,
+                                   int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                                   const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
+                                   void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(P >= 1 && P <= 64, CP_ERR_INVALID_ARG, "P must be in [1, 64]");
+  CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
+  CP_REQUIRE(Hq % P == 0, CP_ERR_SHAPE, "Ulysses needs Hq % P == 0");
+  CP_REQUIRE(ulysses_kv_replicas(Hkv, P) > 0, CP_ERR_SHAPE,
+             "Ulysses needs Hkv % P == 0, or P % Hkv == 0 (key/value heads replicated P/Hkv times)");
+  CP_REQUIRE(S % P == 0, CP_ERR_SHAPE, "Ulysses needs S % P == 0");
+  CP_REQUIRE(S * (int64_t)Hq < (int64_t)INT32_MAX && S * (int64_t)P < (int64_t)INT32_MAX,
+             CP_ERR_UNSUPPORTED, "S*Hq and S*P must be < 2^31");
+  CP_REQUIRE(!cu_seqlens || n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  const size_t es = dtype_size(dtype);
+  const int32_t R = ulysses_kv_replicas(Hkv, P);
+  const int32_t Hqp = Hq / P, Hkvp = Hkv * R / P;
+  CP_REQUIRE(((size_t)Hkvp * D * es) % 16 == 0, CP_ERR_ALIGN,
+             "(Hkv/P)*D*sizeof(dtype) must be a multiple of 16 bytes");
+  if (S == 0) return CP_OK;
+  UlyssesBwdWs w = ulysses_bwd_ws(S, Hq, Hkv, D, dtype, P);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for Ulysses bwd");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(dout, "dout", false);
+  CP_CHECK_T(dq, "dq", false);
+  CP_CHECK_T(dk, "dk", false);
+  CP_CHECK_T(dv, "dv", false);
+  CP_REQUIRE(lse != nullptr, CP_ERR_INVALID_ARG, "lse must not be NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int is_bf16 = dtype == CP_BF16;
+  void* qh = ws_at(workspace, w.q);
+  void* kh = ws_at(workspace, w.k);
+  void* vh = ws_at(workspace, w.v);
+  void* doh = ws_at(workspace, w.dout);
+  float* delta = reinterpret_cast<float*>(ws_at(workspace, w.delta));
+  float* lse_h = reinterpret_cast<float*>(ws_at(workspace, w.lse_h));
+  float* delta_h = reinterpret_cast<float*>(ws_at(workspace, w.delta_h));
+  float* dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
+  float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
+  float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
+  // head_to_seq is the backward of seq_to_head: the gradients take the same
+  // exchange as the outputs.  Delta = rowsum(dO o O) on the sequence layout
+  // (same [Hq, S] order as lse), then both go to the head-major row order.
+  CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
+  CP_TRY(launch_row_gather(kSeq2Head, dout, doh, S, (int64_t)Hq * D * es, P, Hq, st));
+  if (R == 1) {
+    CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+  } else {
+    CP_TRY(launch_kv_replicate(k, kh, S, Hkv, (int64_t)D * es, P, st));
+    CP_TRY(launch_kv_replicate(v, vh, S, Hkv, (int64_t)D * es, P, st));
+  }
+  CP_TRY(launch_bwd_preprocess(out, dout, delta, S, Hq, D, (int32_t)S, is_bf16, st));
+  CP_TRY(launch_lse_to_heads(lse, lse_h, S, Hq, P, st));
+  CP_TRY(launch_lse_to_heads(delta, delta_h, S, Hq, P, st));
+  CP_TRY(launch_zero(dq_acc, (size_t)S * Hq * D * 4, st));
+  // P independent full-sequence problems: key-major schedule, rank p's keys see its queries
+  Schedule* s = new Schedule;
+  s->n_groups = 0;
+  s->n_segs = 0;
+  for (int p = 0; p < P; ++p) {
+    add_group(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
+    add_seg(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
+  }
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = qh; a.k = kh; a.v = vh; a.dout = doh; a.lse = lse_h; a.delta = delta_h;
+  a.dq_acc = dq_acc; a.dk_acc = dk_acc; a.dv_acc = dv_acc;
+  a.q_ld = (int64_t)Hqp * D; a.k_ld = (int64_t)Hkvp * D;
+  a.Hq = Hqp; a.Hkv = Hkvp; a.D = D; a.lse_ld = (int32_t)(P * S);
+  a.scale = 1.0f / sqrtf((float)D);
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.causal = 1; a.cu_seqlens = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0;
+  a.err = device_error_word();
+  cp_status stt = launch_bwd(a, *s, dtype, (int64_t)P * S, (int64_t)P * S, st);
+  delete s;
+  CP_TRY(stt);
+  // back to [S, H, D] in the input dtype; replicated key/value heads sum their copies
+  CP_TRY(launch_heads_to_seq_sum(dq_acc, dq, S, Hq, 1, P, Hqp, D, is_bf16, st));
+  CP_TRY(launch_heads_to_seq_sum(dk_acc, dk, S, Hkv, R, P, Hkvp, D, is_bf16, st));
+  CP_TRY(launch_heads_to_seq_sum(dv_acc, dv, S, Hkv, R, P, Hkvp, D, is_bf16, st));
   return CP_OK;
 }
 

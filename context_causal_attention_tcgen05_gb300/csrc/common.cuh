@@ -123,6 +123,13 @@ cp_status launch_bwd_preprocess(const void* out, const void* dout, float* delta,
                                 int32_t H, int32_t D, int32_t lse_ld, int is_bf16, cudaStream_t st);
 cp_status launch_cast_out(const float* src, void* dst, int64_t n, int is_bf16, cudaStream_t st);
 cp_status launch_zero(void* p, size_t bytes, cudaStream_t st);
+// movers.cu (Ulysses with replicated key/value heads, and the Ulysses backward)
+cp_status launch_kv_replicate(const void* x, void* y, int64_t S, int32_t Hkv, int64_t head_bytes,
+                              int32_t P, cudaStream_t st);
+cp_status launch_lse_to_heads(const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                              cudaStream_t st);
+cp_status launch_heads_to_seq_sum(const float* src, void* dst, int64_t S, int32_t Hd, int32_t R,
+                                  int32_t P, int32_t Hp, int32_t D, int is_bf16, cudaStream_t st);
 cp_status launch_bounded_wait_probe(int32_t timeout_us, int32_t* err, cudaStream_t st);
 // attn_fwd_tc.cu
 cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
@@ -139,6 +146,7 @@ enum GatherKind : int {
   kStripedRestore = 3,
   kSeq2Head = 4,
   kHead2Seq = 5,
+  kSeq2HeadRep = 6,  // Ulysses seq2head of key/value heads replicated P/Hkv times
 };
 
 // Fills group tile prefix sums for a query tile height; returns total units (tiles x heads).

@@ -29,6 +29,7 @@ struct GatherParams {
   uint32_t run_vec;    // vectors per run
   uint32_t P;
   uint32_t a;          // kind-specific: zigzag -> P; striped -> S/P; ulysses -> S
+  uint32_t b;          // replicated seq2head: Hkv
   int kind;
 };
 
@@ -53,6 +54,10 @@ __device__ __forceinline__ uint32_t source_run(const GatherParams& p, uint32_t u
     case kSeq2Head: {  // out run u = rank p*S + s <- in run s*P + p  (run = H/P heads)
       uint32_t rank = u / p.a, s = u - rank * p.a;
       return s * p.P + rank;
+    }
+    case kSeq2HeadRep: {  // out run u = rank p*S + s <- in run s*Hkv + p/(P/Hkv)  (run = one head)
+      uint32_t rank = u / p.a, s = u - rank * p.a;
+      return s * p.b + rank / (p.P / p.b);
     }
     default: {  // kHead2Seq: out run u = s*P + p <- in run p*S + s
       uint32_t s = u / p.P, rank = u - s * p.P;
@@ -123,7 +128,108 @@ __global__ void __launch_bounds__(256) lse_permute_kernel(LsePermParams p) {
   }
 }
 
+// lse-shaped [H, S] fp32 -> the Ulysses head-major order [H/P][P*S]: rank p's
+// heads h' = 0..H/P-1 become heads of one P*S-row problem (row p*S + s).
+__global__ void __launch_bounds__(256) lse_heads_kernel(const float* x, float* y, uint32_t S, uint32_t P,
+                                                        uint32_t Hp, uint64_t total) {
+  for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total; t += (uint64_t)gridDim.x * 256) {
+    const uint64_t PS = (uint64_t)P * S;
+    const uint32_t hp = (uint32_t)(t / PS);
+    const uint64_t rem = t - (uint64_t)hp * PS;
+    const uint32_t rank = (uint32_t)(rem / S), s = (uint32_t)(rem - (uint64_t)rank * S);
+    y[t] = x[((uint64_t)rank * Hp + hp) * S + s];
+  }
+}
+
+// fp32 gradients in the Ulysses layout [P][S][Hp][D] -> [S][Hd][D] in the output
+// dtype, summing the R = P*Hp/Hd consecutive copies of each destination head
+// (R = 1 without replication).  One thread per 16-byte output vector.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) heads_to_seq_sum_kernel(const float* src, void* dst, uint32_t S,
+                                                               uint32_t Hd, uint32_t R, uint32_t Hp,
+                                                               uint32_t D, uint64_t total_vec) {
+  constexpr uint32_t kEpv = kBf16 ? 8 : 4;  // elements per 16-byte output vector
+  const uint32_t vpr = D / kEpv;            // vectors per head row
+  for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total_vec; t += (uint64_t)gridDim.x * 256) {
+    const uint64_t row = t / vpr;  // s * Hd + hd
+    const uint32_t dv = (uint32_t)(t - row * vpr);
+    const uint32_t s = (uint32_t)(row / Hd), hd = (uint32_t)(row - (uint64_t)s * Hd);
+    float acc[kEpv];
+#pragma unroll
+    for (uint32_t e = 0; e < kEpv; ++e) acc[e] = 0.f;
+    for (uint32_t r = 0; r < R; ++r) {
+      const uint32_t g = hd * R + r, rank = g / Hp, hp = g - rank * Hp;
+      const float4* sp = reinterpret_cast<const float4*>(
+          src + (((uint64_t)rank * S + s) * Hp + hp) * D + (uint64_t)dv * kEpv);
+#pragma unroll
+      for (uint32_t e = 0; e < kEpv / 4; ++e) {
+        const float4 f = __ldcs(sp + e);
+        acc[4 * e] += f.x;
+        acc[4 * e + 1] += f.y;
+        acc[4 * e + 2] += f.z;
+        acc[4 * e + 3] += f.w;
+      }
+    }
+    if (kBf16) {
+      uint4 o;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o2[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+      __stcs(reinterpret_cast<uint4*>(dst) + t, o);
+    } else {
+      __stcs(reinterpret_cast<float4*>(dst) + t, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    }
+  }
+}
+
 }  // namespace
+
+cp_status launch_kv_replicate(const void* x, void* y, int64_t S, int32_t Hkv, int64_t head_bytes,
+                              int32_t P, cudaStream_t st) {
+  if (S == 0) return CP_OK;
+  GatherParams p;
+  p.x = static_cast<const int4*>(x);
+  p.y = static_cast<int4*>(y);
+  p.P = (uint32_t)P;
+  p.a = (uint32_t)S;
+  p.b = (uint32_t)Hkv;
+  p.kind = kSeq2HeadRep;
+  p.run_vec = (uint32_t)(head_bytes / 16);
+  const uint64_t total_vec = (uint64_t)P * S * p.run_vec;  // every rank's copy
+  if (total_vec >= (1ull << 32)) {
+    set_last_error("tensor larger than 64 GiB is not supported by the permute kernels");
+    return CP_ERR_UNSUPPORTED;
+  }
+  p.total_vec = (uint32_t)total_vec;
+  uint32_t per_block = kThreads * kVecPerThread;
+  uint32_t blocks = (p.total_vec + per_block - 1) / per_block;
+  row_gather_kernel<<<blocks, kThreads, 0, st>>>(p);
+  return cuda_check(cudaGetLastError(), "row_gather_kernel launch (replicated seq2head)");
+}
+
+cp_status launch_lse_to_heads(const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                              cudaStream_t st) {
+  if (S == 0 || H == 0) return CP_OK;
+  const uint64_t total = (uint64_t)S * H;
+  const uint32_t blocks = (uint32_t)std::min<uint64_t>((total + 255) / 256, 152ull * 16);
+  lse_heads_kernel<<<blocks, 256, 0, st>>>(x, y, (uint32_t)S, (uint32_t)P, (uint32_t)(H / P), total);
+  return cuda_check(cudaGetLastError(), "lse_heads_kernel launch");
+}
+
+cp_status launch_heads_to_seq_sum(const float* src, void* dst, int64_t S, int32_t Hd, int32_t R,
+                                  int32_t P, int32_t Hp, int32_t D, int is_bf16, cudaStream_t st) {
+  if (S == 0) return CP_OK;
+  const uint64_t total_vec = (uint64_t)S * Hd * (D / (is_bf16 ? 8 : 4));
+  const uint32_t blocks = (uint32_t)std::min<uint64_t>((total_vec + 255) / 256, 152ull * 32);
+  (void)P;
+  if (is_bf16)
+    heads_to_seq_sum_kernel<true><<<blocks, 256, 0, st>>>(src, dst, (uint32_t)S, (uint32_t)Hd, (uint32_t)R,
+                                                          (uint32_t)Hp, (uint32_t)D, total_vec);
+  else
+    heads_to_seq_sum_kernel<false><<<blocks, 256, 0, st>>>(src, dst, (uint32_t)S, (uint32_t)Hd, (uint32_t)R,
+                                                           (uint32_t)Hp, (uint32_t)D, total_vec);
+  return cuda_check(cudaGetLastError(), "heads_to_seq_sum_kernel launch");
+}
 
 cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t row_bytes,
                             int32_t P, int32_t H_for_ulysses, cudaStream_t st) {
@@ -132,6 +238,7 @@ cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t
   p.x = static_cast<const int4*>(x);
   p.y = static_cast<int4*>(y);
   p.P = (uint32_t)P;
+  p.b = 0;
   p.kind = kind;
   uint64_t total_bytes = (uint64_t)S * (uint64_t)row_bytes;
   uint64_t total_vec = total_bytes / 16;

@@ -87,7 +87,8 @@ typedef enum {
   CP_OP_RING_BWD = 1,
   CP_OP_ULYSSES_FWD = 2,
   CP_OP_BLOCK_BWD = 3,
-  CP_OP_RING_FWD_REORDERED = 4
+  CP_OP_RING_FWD_REORDERED = 4,
+  CP_OP_ULYSSES_BWD = 5
 } cp_op;
 
 /* Visibility rule of one (query block, key block) pair.
@@ -246,13 +247,34 @@ CP_API cp_status cp_ring_attention_bwd(const void* q, const void* k, const void*
 
 /* Ulysses attention over P virtual ranks ("Ulysses"): seq2head of q, k, v;
  * full-sequence causal attention of each rank's Hq/P query heads (Hkv/P
- * key/value heads); head2seq of out.  Requires Hq % P == 0 and Hkv % P == 0
- * (the degree cannot exceed the key/value head count), S % P == 0.
+ * key/value heads); head2seq of out.  Requires Hq % P == 0, S % P == 0, and
+ * Hkv % P == 0 or P % Hkv == 0: with fewer key/value heads than ranks each
+ * key/value head is replicated P/Hkv times (the chapter's note on grouped
+ * heads under Ulysses), so rank p reads head p / (P/Hkv), the head of its
+ * query heads under the consecutive grouping.  Otherwise CP_ERR_SHAPE.
  * out [S,Hq,D], lse [Hq,S].  workspace >= cp_workspace_size(CP_OP_ULYSSES_FWD). */
 CP_API cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
                                const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward of cp_ulysses_attention ("Ulysses: transposing between the sequence
+ * and the heads"; the pages give no backward: this is the exact gradient of
+ * the definition with the FINAL lse, as for the ring).  head_to_seq is the
+ * backward of seq_to_head, so q, k, v and dout take the forward's exchange,
+ * every rank differentiates its full-sequence attention over its heads, and
+ * dq, dk, dv come back through head_to_seq; replicated key/value heads sum
+ * their copies' gradients.
+ *   q, out, dout: [S,Hq,D]; k, v: [S,Hkv,D]; lse: [Hq,S] fp32 from the forward.
+ *   dq [S,Hq,D], dk/dv [S,Hkv,D]: written (not accumulated), input dtype.
+ *   Same shape rules as cp_ulysses_attention; all device pointers 16-byte
+ *   aligned, caller-owned; workspace >= cp_workspace_size(CP_OP_ULYSSES_BWD)
+ *   (fp32 accumulators and the exchanged tensors).  Asynchronous on `stream`. */
+CP_API cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, const void* out,
+                                          const float* lse, const void* dout, int64_t S, int32_t Hq,
+                                          int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
+                                          const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
+                                          void* dv, void* workspace, size_t ws_bytes, void* stream);
 
 /* Workspace bytes needed by `op` (a cp_op) for these sizes; `mode` is the
  * cp_ring_mode for CP_OP_RING_FWD and ignored otherwise.  For CP_OP_BLOCK_BWD

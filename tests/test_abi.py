@@ -80,12 +80,42 @@ def test_ulysses_refusals(lib):
     f = lib.cp_ulysses_attention
     base = [P16, P16, P16, 32768, 32, 8, 128, 1, 16, None, 0, P16, P16, P16, 1 << 40, None]
     a = list(base)
-    st = f(*a)  # Hkv=8 < P=16: degree limited by the key/value heads
+    a[5] = 6
+    st = f(*a)  # Hkv=6, P=16: neither a divisor nor a multiple of the key/value heads
     assert st == -2 and "Hkv" in cpa.cp_last_error()
     a = list(base)
     a[5] = 32
     a[3] = 32769
     assert f(*a) == -2                                    # S % P
+    a = list(base)  # Hkv=8 < P=16 is accepted (heads replicated): it reaches the workspace check
+    a[14] = 100
+    assert f(*a) == -6
+    need = ctypes.c_size_t()
+    assert lib.cp_workspace_size(2, 32768, 32, 8, 128, 1, 16, 0, ctypes.byref(need)) == 0
+    need_plain = ctypes.c_size_t()
+    assert lib.cp_workspace_size(2, 32768, 32, 16, 128, 1, 16, 0, ctypes.byref(need_plain)) == 0
+    assert need.value == need_plain.value  # 8 heads x 2 copies hold as much as 16 heads
+
+
+def test_ulysses_bwd_refusals(lib):
+    f = lib.cp_ulysses_attention_bwd
+    # q k v out lse dout S Hq Hkv D dtype P cu n_docs dq dk dv ws ws_bytes stream
+    base = [P16, P16, P16, P16, P16, P16, 4096, 32, 8, 128, 1, 16, None, 0, P16, P16, P16, P16, 1 << 40, None]
+    a = list(base)
+    a[8] = 6
+    assert f(*a) == -2 and "Hkv" in cpa.cp_last_error()
+    a = list(base)
+    a[7] = 24                                             # Hq % P
+    assert f(*a) == -2
+    a = list(base)
+    a[18] = 100                                           # workspace too small
+    assert f(*a) == -6
+    a = list(base)
+    a[4] = None                                           # lse required
+    assert f(*a) == -1
+    need = ctypes.c_size_t()
+    assert lib.cp_workspace_size(5, 4096, 32, 8, 128, 1, 16, 0, ctypes.byref(need)) == 0
+    assert need.value > 0
 
 
 def test_permute_refusals(lib):

@@ -95,6 +95,47 @@ def test_ulysses_bf16_medium(Hq, Hkv, P):
     check_ok()
 
 
+@pytest.mark.parametrize("Hq,Hkv,P", [(8, 2, 4), (8, 1, 8), (16, 4, 8)])
+def test_ulysses_replicated_kv_bf16(Hq, Hkv, P):
+    # fewer key/value heads than ranks: each is replicated P/Hkv times before the exchange
+    S, D = 1024, 128
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=16)
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), P)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, "ulysses replicated")
+    check_ok()
+
+
+def test_tiny_exact_ulysses_bwd():
+    # the handbook's tiny workload (fp32, exact path): Ulysses backward vs the plain gradient
+    q, k, v = make_qkv()
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(5))
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), 4)
+    dq, dk, dv = cpa.cp_ulysses_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), 4)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert max_err(got, ref) <= TOL_OUT[torch.float32] * max(1.0, float(np.abs(ref).max())), name
+    check_ok()
+
+
+@pytest.mark.parametrize("Hq,Hkv,P,D,docs", [(8, 8, 4, 128, False), (8, 4, 4, 128, False),
+                                             (8, 2, 4, 128, False), (8, 1, 8, 128, False),
+                                             (8, 4, 2, 128, True), (8, 8, 4, 64, False)])
+def test_ulysses_bwd_bf16_medium(Hq, Hkv, P, D, docs):
+    # the Ulysses backward against the plain gradient of unpartitioned attention
+    S = 512
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=17, with_dout=True)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 300, seed=4)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), P, cu_seqlens=cu_d)
+    dq, dk, dv = cpa.cp_ulysses_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P,
+                                              cu_seqlens=cu_d)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+    check_ok()
+
+
 @pytest.mark.parametrize("layout,docs", [("zigzag", False), ("contiguous", False), ("striped", False),
                                          ("zigzag", True), ("striped", True)])
 def test_ring_bwd_bf16_medium(layout, docs):
@@ -187,6 +228,37 @@ def test_full_gqa_ring_fwd_bwd_s65536_p4_zigzag():
     # identities over all rows (fp64 sums of the GPU result vs of the inputs)
     dv_sum = dv.double().sum(0).cpu().numpy()             # [Hkv, D]
     do_sum = do.double().sum(0).reshape(Hkv, G, D).sum(1).numpy()
+    assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(1.0, np.abs(do_sum).max()), "sum dV"
+    dk_sum = dk.double().sum(0).cpu().numpy()
+    dk_scale = dk.double().abs().sum(0).cpu().numpy().max()
+    assert np.abs(dk_sum).max() <= 1e-3 * dk_scale, "sum dK"
+
+
+def test_full_ulysses_bwd_s32768_h32_p16():
+    """Ulysses forward + backward at S=32768, H=32, D=128, P=16 (the Ulysses shape
+    of the pages' cp=16 runs), checked as the GQA ring backward is: dQ on
+    sampled rows, dK/dV of the last key rows, and the two identities that hold
+    at any size (sum_j dV_j = sum of dO; sum_j dK_j = 0)."""
+    S, H, D, P = 32768, 32, 128, 16
+    q, k, v, do = make_inputs(S, H, H, D, torch.bfloat16, seed=0, with_dout=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, l = cpa.cp_ulysses_attention(qd, kd, vd, P)
+    check_ok()
+    dq, dk, dv = cpa.cp_ulysses_attention_bwd(qd, kd, vd, o, l, dod, P)
+    check_ok()
+    allpos = np.arange(S)
+    rows = sample_rows(S, P, "contiguous", 16)
+    rq, _, _ = oracle.attention_bwd(q[rows], k, v, do[rows], True, pos_q=rows, pos_k=allpos)
+    e = max_err(dq[torch.from_numpy(rows).cuda()], rq)
+    assert e <= 2e-2 * max(1.0, float(np.abs(rq).max())), f"dq {e}"
+    T = 48
+    tail = np.arange(S - T, S)
+    _, rk, rv = oracle.attention_bwd(q[S - T:], k, v, do[S - T:], True, pos_q=tail, pos_k=allpos)
+    for name, got, ref in (("dk", dk[S - T:], rk[S - T:]), ("dv", dv[S - T:], rv[S - T:])):
+        e = max_err(got, ref)
+        assert e <= 2e-2 * max(1.0, float(np.abs(ref).max())), f"{name} {e}"
+    dv_sum = dv.double().sum(0).cpu().numpy()
+    do_sum = do.double().sum(0).numpy()
     assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(1.0, np.abs(do_sum).max()), "sum dV"
     dk_sum = dk.double().sum(0).cpu().numpy()
     dk_scale = dk.double().abs().sum(0).cpu().numpy().max()
