@@ -23,6 +23,7 @@ from .context import (
     ulysses_head2seq,
     ulysses_kv_replicas,
     ulysses_seq2head,
+    usp_attention,
     work,
 )
 
@@ -30,5 +31,5 @@ __all__ = [
     "attention", "attention_bwd", "doc_index", "positions", "visible_mask", "visible_pairs",
     "head_to_seq", "lse_merge", "rank_positions", "rank_visible_pairs", "reorder", "restore",
     "ring_attention", "seq_to_head", "ulysses_attention", "ulysses_attention_bwd", "ulysses_head2seq",
-    "ulysses_kv_replicas", "ulysses_seq2head", "work",
+    "ulysses_kv_replicas", "ulysses_seq2head", "usp_attention", "work",
 ]

@@ -43,6 +43,7 @@ __all__ = [
     "ulysses_attention",
     "ulysses_attention_bwd",
     "ulysses_kv_replicas",
+    "usp_attention",
     "work",
     "rank_visible_pairs",
 ]
@@ -273,6 +274,67 @@ def ulysses_attention_bwd(q, k, v, dout, P: int, causal: bool = True, cu_seqlens
         dk = dk.reshape(S, Hkv, R, -1).sum(axis=2)
         dv = dv.reshape(S, Hkv, R, -1).sum(axis=2)
     return dq, dk, dv
+
+
+def usp_attention(q, k, v, P_ulysses: int, P_ring: int, layout: str = "zigzag", causal: bool = True,
+                  cu_seqlens=None):
+    """Ulysses inside groups of P_ulysses ranks, the ring across P_ring groups
+    (the chapter's note that the two schemes compose: heads are split inside a
+    group, the key/value blocks travel around the ring between groups).
+
+    Group g holds the positions the ring layout gives ring rank g
+    (``rank_positions(S, P_ring, layout)``); inside the group, Ulysses rank u
+    holds the u-th contiguous share of the group's tokens with every head, and
+    ``seq_to_head`` inside the group gives it all of the group's tokens for
+    head share u.  For each head share the ring runs across the groups exactly
+    as in ``ring_attention`` (step s: group g holds the key/value tokens of
+    group (g - s) mod P_ring, merged with lse_merge), and ``head_to_seq``
+    inside the group brings the output back.  Returns (out [S, Hq, D],
+    lse [Hq, S]) in sequence order.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    Pu, Pr = P_ulysses, P_ring
+    assert Hq % Pu == 0 and Hkv % Pu == 0, "Ulysses degree is limited by the head counts"
+    pos = rank_positions(S, Pr, layout)
+    n_g = len(pos[0])
+    assert n_g % Pu == 0
+    Cu = n_g // Pu
+    # the exchange inside each group: head share u of the group's tokens
+    shares = []
+    for g in range(Pr):
+        parts = [(x[pos[g]][r * Cu:(r + 1) * Cu]) for r in range(Pu) for x in (q, k, v)]
+        qh = seq_to_head(parts[0::3], Pu)
+        kh = seq_to_head(parts[1::3], Pu)
+        vh = seq_to_head(parts[2::3], Pu)
+        shares.append((qh, kh, vh))
+    out = np.zeros((S, Hq, D))
+    lse = np.full((Hq, S), -np.inf)
+    Hqu = Hq // Pu
+    for g in range(Pr):
+        outs_g = []
+        for u in range(Pu):
+            qg = shares[g][0][u]
+            o_acc, l_acc = None, None
+            src = g
+            for _step in range(Pr):  # the ring across groups, for head share u
+                ks, vs = shares[src][1][u], shares[src][2][u]
+                if visible_pairs(pos[g], pos[src], causal, cu_seqlens) > 0:
+                    o, l = attention(qg, ks, vs, causal, pos_q=pos[g], pos_k=pos[src], cu_seqlens=cu_seqlens)
+                    if o_acc is None:
+                        o_acc, l_acc = o, l
+                    else:
+                        o_acc, l_acc = lse_merge(o_acc, l_acc, o, l)
+                src = (src - 1) % Pr
+            if o_acc is None:
+                o_acc, l_acc = np.zeros((n_g, Hqu, D)), np.full((Hqu, n_g), -np.inf)
+            outs_g.append(o_acc)
+            lse[u * Hqu:(u + 1) * Hqu, pos[g]] = l_acc
+        out[pos[g]] = np.concatenate(head_to_seq(outs_g, Pu), axis=0)
+    return out, lse
 
 
 def work(query_chunks):

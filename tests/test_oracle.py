@@ -377,6 +377,20 @@ def test_ulysses_bwd_restatement_equals_unpartitioned(Hq, Hkv, P, docs):
         assert np.abs(got - ref).max() < 1e-12
 
 
+@pytest.mark.parametrize("Pu,Pr,layout,Hkv,docs", [(2, 2, "zigzag", 8, None), (2, 3, "contiguous", 4, None),
+                                                    (4, 2, "striped", 8, None), (2, 2, "striped", 2, [9, 20, 19]),
+                                                    (1, 4, "zigzag", 4, None), (4, 1, "contiguous", 4, None)])
+def test_usp_restatement_equals_unpartitioned(Pu, Pr, layout, Hkv, docs):
+    # Ulysses inside groups x ring across groups is plain attention; Pu = 1 is the
+    # ring alone and Pr = 1 Ulysses alone
+    S, Hq, D = 48, 8, 8
+    q, k, v = _rand((S, Hq, D), 120), _rand((S, Hkv, D), 121), _rand((S, Hkv, D), 122)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu)
+    o, l = oracle.usp_attention(q, k, v, Pu, Pr, layout, cu_seqlens=cu)
+    assert np.abs(o - ref_o).max() < 1e-12 and np.abs(l - ref_l).max() < 1e-12
+
+
 def test_ulysses_kv_replicas_counts():
     assert oracle.ulysses_kv_replicas(32, 8, 4) == 1
     assert oracle.ulysses_kv_replicas(32, 8, 16) == 2
