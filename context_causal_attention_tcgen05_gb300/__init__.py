@@ -25,7 +25,7 @@ __all__ = [
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
     "cp_lse_reorder",
     "cp_ring_attention", "cp_ring_attention_reordered", "cp_ring_attention_bwd", "cp_ulysses_attention",
-    "cp_ulysses_attention_bwd",
+    "cp_ulysses_attention_bwd", "cp_usp_attention",
     "cp_workspace_size", "cp_check_device_status", "cp_debug_bounded_wait",
     "cp_status_string", "cp_last_error", "cp_version",
     "CP_F32", "CP_BF16", "REORDER", "RING_MODE", "OP",
@@ -37,7 +37,7 @@ CP_F32, CP_BF16 = 0, 1
 REORDER = {"contiguous": 0, "dual_chunk_swap": 1, "zigzag": 1, "striped": 2, "auto": 3}
 RING_MODE = {"fused": 0, "stepwise": 1}
 OP = {"ring_fwd": 0, "ring_bwd": 1, "ulysses_fwd": 2, "block_bwd": 3, "ring_fwd_reordered": 4,
-      "ulysses_bwd": 5}
+      "ulysses_bwd": 5, "usp_fwd": 6}
 
 _c_i32, _c_i64, _c_f32, _c_p, _c_size = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
@@ -72,6 +72,8 @@ _SIGS = {
                              _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ulysses_attention_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32,
                                  _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
+    "cp_usp_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                         _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_workspace_size": [_c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                           ctypes.POINTER(_c_size)],
     "cp_check_device_status": [_c_p],
@@ -385,6 +387,24 @@ def cp_ulysses_attention_bwd(q, k, v, out, lse, dout, P, cu_seqlens=None, dq=Non
         _ptr(cu_seqlens), n_docs, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return dq, dk, dv
+
+
+def cp_usp_attention(q, k, v, P_ulysses, P_ring, reorder="auto", cu_seqlens=None, out=None, lse=None,
+                     workspace=None, stream=None):
+    """Ulysses inside groups of P_ulysses ranks x the ring across P_ring groups."""
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, S, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(cp_workspace_size("usp_fwd", S, Hq, Hkv, D, q.dtype, P_ring), q.device)
+    n_docs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check("cp_usp_attention", load_library().cp_usp_attention(
+        _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P_ulysses, P_ring, REORDER[reorder],
+        _ptr(cu_seqlens), n_docs, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
 
 
 def cp_check_device_status(stream=None) -> int:

@@ -374,6 +374,28 @@ UlyssesWs ulysses_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtyp
   return w;
 }
 
+// Ulysses inside groups x ring across groups: the ring-ordered q, k, v, their
+// head-major copies (the ring-ordered buffers then hold the head-major output
+// and the head-major q copy the ring-ordered output), and lse in ring order.
+struct UspWs {
+  size_t q_re, k_re, v_re, qh, kh, vh, lse, total;
+};
+UspWs usp_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype) {
+  UspWs w;
+  size_t es = dtype_size(dtype);
+  const size_t nq = (size_t)S * Hq * D * es, nkv = (size_t)S * Hkv * D * es;
+  size_t off = 0;
+  w.q_re = off; off += align_up(nq);
+  w.k_re = off; off += align_up(nkv);
+  w.v_re = off; off += align_up(nkv);
+  w.qh = off; off += align_up(nq);
+  w.kh = off; off += align_up(nkv);
+  w.vh = off; off += align_up(nkv);
+  w.lse = off; off += align_up((size_t)S * Hq * 4);
+  w.total = off;
+  return w;
+}
+
 // Ulysses backward: q, k, v, dout in the head-major layout, lse and Delta in the
 // head-major row order, fp32 gradient accumulators in the head-major layout.
 struct UlyssesBwdWs {
@@ -695,6 +717,9 @@ cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hkv, int3
     case CP_OP_ULYSSES_BWD:
       *bytes = ulysses_bwd_ws(S, Hq, Hkv, D, dtype, P).total;
       return CP_OK;
+    case CP_OP_USP_FWD:  // independent of the degrees
+      *bytes = usp_ws(S, Hq, Hkv, D, dtype).total;
+      return CP_OK;
     case CP_OP_BLOCK_BWD:  // S is max(Sq, Sk) here
       *bytes = block_bwd_ws(S, S, Hq, Hkv, D).total;
       return CP_OK;
@@ -927,6 +952,102 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   delete s;
   CP_TRY(stt);
   CP_TRY(launch_row_gather(kHead2Seq, oh, out, S, (int64_t)Hq * D * es, P, Hq, st));
+  return CP_OK;
+}
+
+cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                           int32_t Hkv, int32_t D, int32_t dtype, int32_t P_ulysses, int32_t P_ring,
+                           int32_t reorder, const int32_t* cu_seqlens, int32_t n_docs, void* out,
+                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  CP_REQUIRE(reorder >= CP_REORDER_CONTIGUOUS && reorder <= CP_REORDER_AUTO, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  CP_REQUIRE(P_ulysses >= 1 && P_ring >= 1 && P_ulysses * P_ring <= 64, CP_ERR_INVALID_ARG,
+             "P_ulysses, P_ring >= 1 and P_ulysses * P_ring <= 64 required");
+  const int32_t layout = resolve_layout(reorder, cu_seqlens);
+  CP_TRY(check_ring_args(S, Hq, Hkv, D, dtype, P_ring, layout, cu_seqlens, n_docs));
+  CP_REQUIRE(Hq % P_ulysses == 0 && Hkv % P_ulysses == 0, CP_ERR_SHAPE,
+             "USP needs Hq % P_ulysses == 0 and Hkv % P_ulysses == 0");
+  CP_REQUIRE((S / P_ring) % P_ulysses == 0, CP_ERR_SHAPE,
+             "USP needs each ring group's tokens (S / P_ring) to split evenly over P_ulysses ranks");
+  const size_t es = dtype_size(dtype);
+  const int32_t Hqp = Hq / P_ulysses, Hkvp = Hkv / P_ulysses;
+  CP_REQUIRE(((size_t)Hkvp * D * es) % 16 == 0, CP_ERR_ALIGN,
+             "(Hkv/P_ulysses)*D*sizeof(dtype) must be a multiple of 16 bytes");
+  if (S == 0) return CP_OK;
+  UspWs w = usp_ws(S, Hq, Hkv, D, dtype);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for USP");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool moved = layout != CP_REORDER_CONTIGUOUS;
+  const int fwd_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagReorder : kStripedReorder;
+  const int back_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagRestore : kStripedRestore;
+  const void *q_re = q, *k_re = k, *v_re = v;
+  if (moved) {  // the ring's partition across groups
+    CP_TRY(launch_row_gather(fwd_kind, q, ws_at(workspace, w.q_re), S, (int64_t)Hq * D * es, P_ring, Hq, st));
+    CP_TRY(launch_row_gather(fwd_kind, k, ws_at(workspace, w.k_re), S, (int64_t)Hkv * D * es, P_ring, Hkv, st));
+    CP_TRY(launch_row_gather(fwd_kind, v, ws_at(workspace, w.v_re), S, (int64_t)Hkv * D * es, P_ring, Hkv, st));
+    q_re = ws_at(workspace, w.q_re);
+    k_re = ws_at(workspace, w.k_re);
+    v_re = ws_at(workspace, w.v_re);
+  }
+  // the exchange inside each group: head share u of every token (the ring order is kept)
+  void* qh = ws_at(workspace, w.qh);
+  void* kh = ws_at(workspace, w.kh);
+  void* vh = ws_at(workspace, w.vh);
+  CP_TRY(launch_row_gather(kSeq2Head, q_re, qh, S, (int64_t)Hq * D * es, P_ulysses, Hq, st));
+  CP_TRY(launch_row_gather(kSeq2Head, k_re, kh, S, (int64_t)Hkv * D * es, P_ulysses, Hkv, st));
+  CP_TRY(launch_row_gather(kSeq2Head, v_re, vh, S, (int64_t)Hkv * D * es, P_ulysses, Hkv, st));
+  // the fused ring across groups, once per head share, in one launch
+  Schedule* ring = new Schedule;
+  Schedule* s = new Schedule;
+  build_ring_schedule(*ring, S, P_ring, layout, -1, 1);
+  if ((int64_t)ring->n_groups * P_ulysses > kMaxGroups || (int64_t)ring->n_segs * P_ulysses > kMaxSegs) {
+    delete ring;
+    delete s;
+    set_last_error("USP schedule too large (ring groups x P_ulysses exceeds the schedule capacity)");
+    return CP_ERR_UNSUPPORTED;
+  }
+  s->n_groups = 0;
+  s->n_segs = 0;
+  for (int u = 0; u < P_ulysses; ++u)
+    for (int gi = 0; gi < ring->n_groups; ++gi) {
+      const QGroup& rg = ring->g[gi];
+      QGroup& g = s->g[s->n_groups++];
+      g = rg;
+      g.q_row0 = rg.q_row0 + u * (int32_t)S;
+      g.o_row0 = rg.o_row0 + u * (int32_t)S;
+      g.lse_head0 = rg.lse_head0 + u * Hqp;  // lse columns stay in ring order
+      g.seg_begin = s->n_segs;
+      for (int si = 0; si < rg.seg_count; ++si) {
+        KSeg sg = ring->s[rg.seg_begin + si];
+        sg.k_row0 += u * (int32_t)S;
+        s->s[s->n_segs++] = sg;
+      }
+    }
+  sort_groups_by_work(*s);
+  delete ring;
+  // outputs: head-major into the ring-ordered q buffer (free after seq2head, or never used
+  // when the layout is contiguous), lse in ring order
+  void* oh = ws_at(workspace, w.q_re);
+  float* lse_re = moved ? reinterpret_cast<float*>(ws_at(workspace, w.lse)) : lse;
+  AttnArgs a = make_fwd_args(qh, kh, vh, oh, lse_re, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
+                             1.0f / sqrtf((float)D), 0);
+  cp_status stt = launch_fwd(a, *s, dtype, (int64_t)P_ulysses * S, (int64_t)P_ulysses * S, st);
+  delete s;
+  CP_TRY(stt);
+  if (moved) {
+    void* o_re = ws_at(workspace, w.qh);  // free after the attention
+    CP_TRY(launch_row_gather(kHead2Seq, oh, o_re, S, (int64_t)Hq * D * es, P_ulysses, Hq, st));
+    CP_TRY(launch_row_gather(back_kind, o_re, out, S, (int64_t)Hq * D * es, P_ring, Hq, st));
+    CP_TRY(launch_lse_permute(back_kind, lse_re, lse, S, Hq, P_ring, st));
+  } else {
+    CP_TRY(launch_row_gather(kHead2Seq, oh, out, S, (int64_t)Hq * D * es, P_ulysses, Hq, st));
+  }
   return CP_OK;
 }
 

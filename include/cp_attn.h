@@ -88,7 +88,8 @@ typedef enum {
   CP_OP_ULYSSES_FWD = 2,
   CP_OP_BLOCK_BWD = 3,
   CP_OP_RING_FWD_REORDERED = 4,
-  CP_OP_ULYSSES_BWD = 5
+  CP_OP_ULYSSES_BWD = 5,
+  CP_OP_USP_FWD = 6
 } cp_op;
 
 /* Visibility rule of one (query block, key block) pair.
@@ -257,6 +258,24 @@ CP_API cp_status cp_ulysses_attention(const void* q, const void* k, const void* 
                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
                                const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Ulysses inside groups of P_ulysses ranks, the ring across P_ring groups (the
+ * chapter's note that the two schemes compose: "Ulysses" splits the heads
+ * inside a group, "Ring Attention" passes the key/value blocks between
+ * groups).  Ring rank g's positions (reorder over P_ring, as in
+ * cp_ring_attention) form group g; inside it the exchange gives each of the
+ * P_ulysses ranks all of the group's tokens for Hq/P_ulysses heads; the FUSED
+ * ring then runs across groups for every head share (one launch for all).
+ *   q [S,Hq,D], k/v [S,Hkv,D] in sequence order; out [S,Hq,D], lse [Hq,S].
+ *   Ring rules as cp_ring_attention with P = P_ring; Hq % P_ulysses == 0,
+ *   Hkv % P_ulysses == 0, (S / P_ring) % P_ulysses == 0 (CP_ERR_SHAPE), and
+ *   P_ulysses * P_ring <= 64.  workspace >= cp_workspace_size(CP_OP_USP_FWD)
+ *   (independent of the degrees).  Caller-owned device pointers, 16-byte
+ *   aligned; asynchronous on `stream`. */
+CP_API cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t dtype, int32_t P_ulysses, int32_t P_ring,
+                                  int32_t reorder, const int32_t* cu_seqlens, int32_t n_docs, void* out,
+                                  float* lse, void* workspace, size_t ws_bytes, void* stream);
 
 /* Backward of cp_ulysses_attention ("Ulysses: transposing between the sequence
  * and the heads"; the pages give no backward: this is the exact gradient of

@@ -97,6 +97,26 @@ def test_ulysses_refusals(lib):
     assert need.value == need_plain.value  # 8 heads x 2 copies hold as much as 16 heads
 
 
+def test_usp_refusals(lib):
+    f = lib.cp_usp_attention
+    # q k v S Hq Hkv D dtype Pu Pr reorder cu n_docs out lse ws ws_bytes stream
+    base = [P16, P16, P16, 8192, 32, 8, 128, 1, 4, 4, 1, None, 0, P16, P16, P16, 1 << 40, None]
+    a = list(base)
+    a[5] = 6                                              # Hkv % P_ulysses
+    assert f(*a) == -2
+    a = list(base)
+    a[8], a[9] = 8, 16                                    # P_ulysses * P_ring > 64
+    assert f(*a) == -1
+    a = list(base)
+    a[3] = 40                                             # zigzag rule holds, (S / P_ring) % P_ulysses does not
+    assert f(*a) == -2
+    a = list(base)
+    a[16] = 100                                           # workspace too small
+    assert f(*a) == -6
+    need = ctypes.c_size_t()
+    assert lib.cp_workspace_size(6, 8192, 32, 8, 128, 1, 4, 0, ctypes.byref(need)) == 0 and need.value > 0
+
+
 def test_ulysses_bwd_refusals(lib):
     f = lib.cp_ulysses_attention_bwd
     # q k v out lse dout S Hq Hkv D dtype P cu n_docs dq dk dv ws ws_bytes stream

@@ -136,6 +136,30 @@ def test_ulysses_bwd_bf16_medium(Hq, Hkv, P, D, docs):
     check_ok()
 
 
+@pytest.mark.parametrize("Pu,Pr,layout", [(2, 2, "contiguous"), (2, 2, "zigzag"), (4, 2, "striped"), (1, 4, "zigzag"),
+                                          (4, 1, "contiguous")])
+def test_tiny_exact_usp(Pu, Pr, layout):
+    # the handbook's tiny workload (fp32) through Ulysses-inside-groups x ring-across-groups
+    q, k, v = make_qkv()
+    ref_o, ref_l = oracle.attention(q, k, v, True)
+    o, l = cpa.cp_usp_attention(q.cuda(), k.cuda(), v.cuda(), Pu, Pr, layout)
+    assert_close(o, l, ref_o, ref_l, torch.float32, f"usp {Pu}x{Pr} {layout}")
+    check_ok()
+
+
+@pytest.mark.parametrize("Pu,Pr,layout,Hkv,docs", [(2, 4, "zigzag", 4, False), (4, 2, "striped", 8, True),
+                                                   (2, 2, "contiguous", 2, False), (2, 4, "zigzag", 2, True)])
+def test_usp_bf16_medium(Pu, Pr, layout, Hkv, docs):
+    S, Hq, D = 2048, 8, 128
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=18)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 700, seed=5)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu)
+    o, l = cpa.cp_usp_attention(q.cuda(), k.cuda(), v.cuda(), Pu, Pr, layout, cu_seqlens=cu_d)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"usp {Pu}x{Pr} {layout}")
+    check_ok()
+
+
 @pytest.mark.parametrize("layout,docs", [("zigzag", False), ("contiguous", False), ("striped", False),
                                          ("zigzag", True), ("striped", True)])
 def test_ring_bwd_bf16_medium(layout, docs):
