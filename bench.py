@@ -52,6 +52,22 @@ def _dist():
     return ws, rank
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (time-like numbers), identical on every rank;
+    the input itself on one process."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, ms: float) -> float:
+    """Throughput of the whole job: every rank processed flop_per_rank in at most ms."""
+    return world * flop_per_rank / (ms * 1e-3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -446,13 +462,9 @@ def bench_ours(args):
     step_ms = [e[0].elapsed_time(e[3]) for e in events]
     attn_ms = [e[1].elapsed_time(e[2]) for e in events]
     perm_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in events]
-    mean_step = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([mean_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_step = float(t.item())
+    mean_step = max_over_ranks(statistics.mean(step_ms), dev)
     flop = causal_flop(S, H, D)
-    value = ws * flop / (mean_step * 1e-3) / 1e12
+    value = whole_job_tflops(flop, ws, mean_step)
     attn_mean = statistics.mean(attn_ms)
     achieved = flop / (attn_mean * 1e-3) / 1e12
     tensor_bytes = S * H * D * 2
@@ -531,11 +543,8 @@ def bench_ours(args):
     st = cpa.cp_check_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st}: {cpa.cp_last_error()}")
-    if ws > 1:
-        t = torch.tensor([e2e_mean], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_mean = float(t.item())
-    e2e_value = ws * flop / (e2e_mean * 1e-3) / 1e12
+    e2e_mean = max_over_ranks(e2e_mean, dev)
+    e2e_value = whole_job_tflops(flop, ws, e2e_mean)
 
     if rank == 0:
         peaks = _peaks()
