@@ -55,17 +55,24 @@ def doc_index(pos: np.ndarray, cu_seqlens) -> np.ndarray:
     return np.searchsorted(cu, pos, side="right") - 1
 
 
-def visible_mask(pos_q: np.ndarray, pos_k: np.ndarray, causal: bool = True, cu_seqlens=None) -> np.ndarray:
+def visible_mask(pos_q: np.ndarray, pos_k: np.ndarray, causal: bool = True, cu_seqlens=None,
+                 window: int = 0) -> np.ndarray:
     """Boolean [Sq, Sk]: True where query i may attend to key j.
 
     Causal rule from the handbook's ``attention``: masked when key position > query position.
     Document rule (packing): masked when the two positions lie in different documents.
+    Sliding window (window > 0, with the causal rule; the transformers pull request's
+    mask tests): masked when the key lies window or more positions before the query,
+    so a query sees itself and the window - 1 keys before it.
     """
     pq = np.asarray(pos_q, dtype=np.int64)[:, None]
     pk = np.asarray(pos_k, dtype=np.int64)[None, :]
     vis = np.ones((pq.shape[0], pk.shape[1]), dtype=bool)
     if causal:
         vis &= ~(pk > pq)
+    if window:
+        assert causal, "a sliding window is defined with the causal rule"
+        vis &= (pq - pk) < window
     if cu_seqlens is not None:
         vis &= doc_index(pq, cu_seqlens) == doc_index(pk, cu_seqlens)
     return vis
@@ -92,7 +99,7 @@ def _resolve_positions(Sq, Sk, q_offset, k_offset, q_stride, k_stride, pos_q, po
 
 def attention(q, k, v, causal: bool = True, q_offset: int = 0, k_offset: int = 0, *,
               q_stride: int = 1, k_stride: int = 1, pos_q=None, pos_k=None,
-              cu_seqlens=None, scale: float | None = None, row_block: int = 1024):
+              cu_seqlens=None, scale: float | None = None, row_block: int = 1024, window: int = 0):
     """Forward attention of one (query block, key/value block) pair.
 
     q: [Sq, Hq, D]; k, v: [Sk, Hkv, D] (any real dtype; computed in float64).
@@ -118,7 +125,7 @@ def attention(q, k, v, causal: bool = True, q_offset: int = 0, k_offset: int = 0
         return out, lse
     for i0 in range(0, Sq, row_block):
         i1 = min(Sq, i0 + row_block)
-        vis = visible_mask(pos_q[i0:i1], pos_k, causal, cu_seqlens)
+        vis = visible_mask(pos_q[i0:i1], pos_k, causal, cu_seqlens, window)
         any_vis = vis.any(axis=1)
         for h in range(Hq):
             hk = h // G
@@ -138,7 +145,7 @@ def attention(q, k, v, causal: bool = True, q_offset: int = 0, k_offset: int = 0
 
 def attention_bwd(q, k, v, dout, causal: bool = True, q_offset: int = 0, k_offset: int = 0, *,
                   q_stride: int = 1, k_stride: int = 1, pos_q=None, pos_k=None,
-                  cu_seqlens=None, scale: float | None = None, row_block: int = 1024):
+                  cu_seqlens=None, scale: float | None = None, row_block: int = 1024, window: int = 0):
     """Gradients (dq, dk, dv) of sum(dout * out) for ``attention`` above, float64.
 
     With P = softmax of the visible scores and O = P v:
@@ -165,7 +172,7 @@ def attention_bwd(q, k, v, dout, causal: bool = True, q_offset: int = 0, k_offse
     dv = np.zeros_like(v)
     for i0 in range(0, Sq, row_block):
         i1 = min(Sq, i0 + row_block)
-        vis = visible_mask(pos_q[i0:i1], pos_k, causal, cu_seqlens)
+        vis = visible_mask(pos_q[i0:i1], pos_k, causal, cu_seqlens, window)
         any_vis = vis.any(axis=1)
         for h in range(Hq):
             hk = h // G
@@ -186,6 +193,6 @@ def attention_bwd(q, k, v, dout, causal: bool = True, q_offset: int = 0, k_offse
     return dq, dk, dv
 
 
-def visible_pairs(pos_q, pos_k, causal: bool = True, cu_seqlens=None) -> int:
+def visible_pairs(pos_q, pos_k, causal: bool = True, cu_seqlens=None, window: int = 0) -> int:
     """Number of visible (query, key) pairs of one block pair (per head)."""
-    return int(visible_mask(pos_q, pos_k, causal, cu_seqlens).sum())
+    return int(visible_mask(pos_q, pos_k, causal, cu_seqlens, window).sum())

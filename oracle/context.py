@@ -220,7 +220,7 @@ def _ulysses_inputs(q, k, v, P: int):
     return q, k, v, R
 
 
-def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None):
+def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None, window: int = 0):
     """The Ulysses scheme over P virtual ranks, restated from the Ulysses section.
 
     Each rank's slice of q, k, v goes through ``seq_to_head``; rank p runs
@@ -237,7 +237,7 @@ def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None):
     vh = seq_to_head([v[s] for s in sl], P)
     outs, lses = [], []
     for p in range(P):
-        o, l = attention(qh[p], kh[p], vh[p], causal, cu_seqlens=cu_seqlens)
+        o, l = attention(qh[p], kh[p], vh[p], causal, cu_seqlens=cu_seqlens, window=window)
         outs.append(o)
         lses.append(l)
     out = np.concatenate(head_to_seq(outs, P), axis=0)
@@ -245,7 +245,7 @@ def ulysses_attention(q, k, v, P: int, causal: bool = True, cu_seqlens=None):
     return out, lse
 
 
-def ulysses_attention_bwd(q, k, v, dout, P: int, causal: bool = True, cu_seqlens=None):
+def ulysses_attention_bwd(q, k, v, dout, P: int, causal: bool = True, cu_seqlens=None, window: int = 0):
     """Backward of the Ulysses scheme, restated rank by rank.
 
     head_to_seq is the backward of seq_to_head (a permutation), so the gradients
@@ -263,7 +263,8 @@ def ulysses_attention_bwd(q, k, v, dout, P: int, causal: bool = True, cu_seqlens
     qh, kh, vh, doh = (seq_to_head([x[s] for s in sl], P) for x in (q, k, v, dout))
     dqs, dks, dvs = [], [], []
     for p in range(P):
-        dq_p, dk_p, dv_p = attention_bwd(qh[p], kh[p], vh[p], doh[p], causal, cu_seqlens=cu_seqlens)
+        dq_p, dk_p, dv_p = attention_bwd(qh[p], kh[p], vh[p], doh[p], causal, cu_seqlens=cu_seqlens,
+                                         window=window)
         dqs.append(dq_p)
         dks.append(dk_p)
         dvs.append(dv_p)

@@ -391,6 +391,70 @@ def test_usp_restatement_equals_unpartitioned(Pu, Pr, layout, Hkv, docs):
     assert np.abs(o - ref_o).max() < 1e-12 and np.abs(l - ref_l).max() < 1e-12
 
 
+def _window_mask(pos_q, pos_k, window, cu=None):
+    """Sliding-window visibility by scalar loops: key not after the query, fewer than
+    `window` positions before it, same document."""
+    m = np.zeros((len(pos_q), len(pos_k)), dtype=bool)
+    for i, a in enumerate(pos_q):
+        for j, b in enumerate(pos_k):
+            same = True if cu is None else (np.searchsorted(cu, a, "right") == np.searchsorted(cu, b, "right"))
+            m[i, j] = (b <= a) and (a - b < window) and same
+    return m
+
+
+@pytest.mark.parametrize("window,docs", [(1, None), (3, None), (7, [5, 9, 6]), (40, None)])
+def test_sliding_window_against_sdpa_and_brute_force(window, docs):
+    S, Hq, Hkv, D = 20, 4, 2, 8
+    q, k, v = _rand((S, Hq, D), 130), _rand((S, Hkv, D), 131), _rand((S, Hkv, D), 132)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    pos = np.arange(S)
+    mask = _window_mask(pos, pos, window, cu)
+    assert np.array_equal(oattn_mod.visible_mask(pos, pos, True, cu, window), mask)
+    o, l = oracle.attention(q, k, v, True, cu_seqlens=cu, window=window)
+    assert np.abs(o - _sdpa(q, k, v, mask=mask)).max() < 1e-12
+    if window >= S and docs is None:  # a window longer than the sequence is plain causal attention
+        ref_o, ref_l = oracle.attention(q, k, v, True)
+        assert np.abs(o - ref_o).max() < 1e-13 and np.abs(l - ref_l).max() < 1e-13
+
+
+def test_sliding_window_of_one_is_the_diagonal():
+    # each query sees only itself: out = its own value row, lse = its own scaled score
+    S, H, D = 9, 2, 4
+    q, k, v = _rand((S, H, D), 133), _rand((S, H, D), 134), _rand((S, H, D), 135)
+    o, l = oracle.attention(q, k, v, True, window=1)
+    assert np.abs(o - v).max() < 1e-14
+    assert np.abs(l - (np.sum(q * k, axis=2) / math.sqrt(D)).T).max() < 1e-13
+
+
+def test_sliding_window_bwd_matches_autograd():
+    S, Hq, Hkv, D, W = 15, 4, 2, 8, 5
+    q, k, v, do = (_rand((S, Hq, D), 136), _rand((S, Hkv, D), 137), _rand((S, Hkv, D), 138),
+                   _rand((S, Hq, D), 139))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, True, window=W)
+    mask = torch.from_numpy(_window_mask(np.arange(S), np.arange(S), W))
+    qt, kt, vt = (torch.from_numpy(x).requires_grad_() for x in (q, k, v))
+    G = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt.permute(1, 0, 2)[None], kt.repeat_interleave(G, 1).permute(1, 0, 2)[None],
+        vt.repeat_interleave(G, 1).permute(1, 0, 2)[None], attn_mask=mask)[0].permute(1, 0, 2)
+    (o * torch.from_numpy(do)).sum().backward()
+    for got, ref in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        assert np.abs(got - ref.numpy()).max() < 1e-11
+
+
+def test_ulysses_with_window_equals_unpartitioned():
+    S, Hq, Hkv, D, P, W = 24, 8, 2, 8, 4, 6
+    q, k, v, do = (_rand((S, Hq, D), 140), _rand((S, Hkv, D), 141), _rand((S, Hkv, D), 142),
+                   _rand((S, Hq, D), 143))
+    ref_o, ref_l = oracle.attention(q, k, v, True, window=W)
+    o, l = oracle.ulysses_attention(q, k, v, P, window=W)
+    assert np.abs(o - ref_o).max() < 1e-12 and np.abs(l - ref_l).max() < 1e-12
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, window=W)
+    dq, dk, dv = oracle.ulysses_attention_bwd(q, k, v, do, P, window=W)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert np.abs(got - ref).max() < 1e-12
+
+
 def test_ulysses_kv_replicas_counts():
     assert oracle.ulysses_kv_replicas(32, 8, 4) == 1
     assert oracle.ulysses_kv_replicas(32, 8, 16) == 2
@@ -454,8 +518,8 @@ def test_planted_mistakes_are_caught(monkeypatch):
     # an off-by-one causal mask (key at the query's own position hidden)
     orig = oattn_mod.visible_mask
 
-    def shifted(pq, pk, causal=True, cu=None):
-        m = orig(pq, pk, causal, cu)
+    def shifted(pq, pk, causal=True, cu=None, window=0):
+        m = orig(pq, pk, causal, cu, window)
         pq_ = np.asarray(pq)[:, None]
         pk_ = np.asarray(pk)[None, :]
         return m & ~(pk_ == pq_) | (m & False)
