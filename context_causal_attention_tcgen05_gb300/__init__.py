@@ -44,7 +44,8 @@ _c_i32, _c_i64, _c_f32, _c_p, _c_size = ctypes.c_int32, ctypes.c_int64, ctypes.c
 
 class cp_mask(ctypes.Structure):
     _fields_ = [("causal", _c_i32), ("q_offset", _c_i64), ("k_offset", _c_i64),
-                ("q_stride", _c_i64), ("k_stride", _c_i64), ("cu_seqlens", _c_p), ("n_docs", _c_i32)]
+                ("q_stride", _c_i64), ("k_stride", _c_i64), ("cu_seqlens", _c_p), ("n_docs", _c_i32),
+                ("window", _c_i32)]
 
 
 _SIGS = {
@@ -69,9 +70,9 @@ _SIGS = {
     "cp_ring_attention_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32,
                               _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ulysses_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p,
-                             _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
+                             _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ulysses_attention_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32,
-                                 _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
+                                 _c_i32, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_usp_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                          _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_workspace_size": [_c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
@@ -156,9 +157,10 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _mask(causal=True, q_offset=0, k_offset=0, q_stride=1, k_stride=1, cu_seqlens=None):
+def _mask(causal=True, q_offset=0, k_offset=0, q_stride=1, k_stride=1, cu_seqlens=None, window=0):
     m = cp_mask()
     m.causal = int(bool(causal))
+    m.window = int(window)
     m.q_offset, m.k_offset = int(q_offset), int(k_offset)
     m.q_stride, m.k_stride = int(q_stride), int(k_stride)
     if cu_seqlens is not None:
@@ -184,7 +186,7 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def cp_attn_block_fwd(q, k, v, causal=True, q_offset=0, k_offset=0, q_stride=1, k_stride=1,
-                      cu_seqlens=None, scale=0.0, out=None, lse=None, stream=None):
+                      cu_seqlens=None, scale=0.0, out=None, lse=None, stream=None, window=0):
     """out [Sq,Hq,D], lse [Hq,Sq] (fp32) of one block pair."""
     Sq, Hq, D = q.shape
     Sk, Hkv, _ = k.shape
@@ -192,7 +194,7 @@ def cp_attn_block_fwd(q, k, v, causal=True, q_offset=0, k_offset=0, q_stride=1, 
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(Hq, Sq, dtype=torch.float32, device=q.device)
-    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens)
+    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens, window)
     _check("cp_attn_block_fwd", load_library().cp_attn_block_fwd(
         _ptr(q), _ptr(k), _ptr(v), Sq, Sk, Hq, Hkv, D, _dt(q), ctypes.byref(m), float(scale),
         _ptr(out), _ptr(lse), _stream(stream)))
@@ -200,13 +202,13 @@ def cp_attn_block_fwd(q, k, v, causal=True, q_offset=0, k_offset=0, q_stride=1, 
 
 
 def cp_attn_block_bwd(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0, q_stride=1,
-                      k_stride=1, cu_seqlens=None, scale=0.0, stream=None):
+                      k_stride=1, cu_seqlens=None, scale=0.0, stream=None, window=0):
     """(dq, dk, dv) of one block pair given the final out and lse."""
     Sq, Hq, D = q.shape
     Sk, Hkv, _ = k.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = _workspace(cp_workspace_size("block_bwd", max(Sq, Sk), Hq, Hkv, D, q.dtype, 1), q.device)
-    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens)
+    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens, window)
     _check("cp_attn_block_bwd", load_library().cp_attn_block_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
         ctypes.byref(m), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
@@ -216,7 +218,7 @@ def cp_attn_block_bwd(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset
 
 def cp_attn_block_bwd_noalloc(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0,
                               q_stride=1, k_stride=1, cu_seqlens=None, scale=0.0, dq=None, dk=None,
-                              dv=None, stream=None):
+                              dv=None, stream=None, window=0):
     """cp_attn_block_bwd without a workspace: the library uses its built-in
     32 MiB scratch array and allocates nothing (outputs are allocated here
     unless passed in)."""
@@ -225,7 +227,7 @@ def cp_attn_block_bwd_noalloc(q, k, v, out, dout, lse, causal=True, q_offset=0, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens)
+    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens, window)
     _check("cp_attn_block_bwd_noalloc", load_library().cp_attn_block_bwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
         ctypes.byref(m), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
@@ -355,7 +357,8 @@ def cp_ring_attention_bwd(q, k, v, out, lse, dout, P, reorder="auto", cu_seqlens
     return dq, dk, dv
 
 
-def cp_ulysses_attention(q, k, v, P, cu_seqlens=None, out=None, lse=None, workspace=None, stream=None):
+def cp_ulysses_attention(q, k, v, P, cu_seqlens=None, out=None, lse=None, workspace=None, stream=None,
+                         window=0):
     S, Hq, D = q.shape
     Hkv = k.shape[1]
     if out is None:
@@ -366,13 +369,13 @@ def cp_ulysses_attention(q, k, v, P, cu_seqlens=None, out=None, lse=None, worksp
         workspace = _workspace(cp_workspace_size("ulysses_fwd", S, Hq, Hkv, D, q.dtype, P), q.device)
     n_docs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     _check("cp_ulysses_attention", load_library().cp_ulysses_attention(
-        _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P, _ptr(cu_seqlens), n_docs, _ptr(out),
-        _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P, _ptr(cu_seqlens), n_docs, int(window),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
 
 
 def cp_ulysses_attention_bwd(q, k, v, out, lse, dout, P, cu_seqlens=None, dq=None, dk=None, dv=None,
-                             workspace=None, stream=None):
+                             workspace=None, stream=None, window=0):
     """Backward of cp_ulysses_attention: (dq, dk, dv) from the forward's out and lse."""
     S, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -384,8 +387,8 @@ def cp_ulysses_attention_bwd(q, k, v, out, lse, dout, P, cu_seqlens=None, dq=Non
     n_docs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     _check("cp_ulysses_attention_bwd", load_library().cp_ulysses_attention_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), S, Hq, Hkv, D, _dt(q), P,
-        _ptr(cu_seqlens), n_docs, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-        _stream(stream)))
+        _ptr(cu_seqlens), n_docs, int(window), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return dq, dk, dv
 
 

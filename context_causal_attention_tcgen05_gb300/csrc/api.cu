@@ -515,9 +515,11 @@ cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t
   CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
   CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
              CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
-  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0};
+  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0, 0};
   if (mask) m = *mask;
   CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  CP_REQUIRE(m.window >= 0, CP_ERR_INVALID_ARG, "mask window must be >= 0");
+  CP_REQUIRE(m.window == 0 || m.causal, CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
   CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
                  fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
                  fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
@@ -538,6 +540,7 @@ cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t
   if (Sk > 0) add_seg(*s, Piece{0, (int32_t)Sk, (int32_t)m.k_offset, (int32_t)m.k_stride});
   AttnArgs a = make_fwd_args(q, k, v, out, lse, Hq, Hkv, D, Sq, m.causal, m.cu_seqlens, m.n_docs,
                              scale, 0);
+  a.window = m.window;
   cp_status st = launch_fwd(a, *s, dtype, Sq, Sk, (cudaStream_t)stream);
   delete s;
   return st;
@@ -552,9 +555,11 @@ cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const v
   CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
   CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
              CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
-  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0};
+  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0, 0};
   if (mask) m = *mask;
   CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  CP_REQUIRE(m.window >= 0, CP_ERR_INVALID_ARG, "mask window must be >= 0");
+  CP_REQUIRE(m.window == 0 || m.causal, CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
   CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
                  fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
                  fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
@@ -597,6 +602,7 @@ cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const v
   a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)Sq;
   a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
+  a.window = m.window;
   a.err = device_error_word();
   cp_status stt = launch_bwd(a, *s, dtype, Sq, Sk, st);
   delete s;
@@ -898,8 +904,9 @@ cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, con
 
 cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
-                               const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               const int32_t* cu_seqlens, int32_t n_docs, int32_t window, void* out,
+                               float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  CP_REQUIRE(window >= 0, CP_ERR_INVALID_ARG, "window must be >= 0");
   CP_TRY(check_common(Hq, Hkv, D, dtype));
   CP_REQUIRE(P >= 1 && P <= 64, CP_ERR_INVALID_ARG, "P must be in [1, 64]");
   CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
@@ -948,6 +955,7 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   }
   AttnArgs a = make_fwd_args(qh, kh, vh, oh, lse, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
                              1.0f / sqrtf((float)D), 0);
+  a.window = window;
   cp_status stt = launch_fwd(a, *s, dtype, (int64_t)P * S, (int64_t)P * S, st);
   delete s;
   CP_TRY(stt);
@@ -1054,9 +1062,10 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
 cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, const void* out,
                                    const float* lse, const void* dout, int64_t S, int32_t Hq,
                                    int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
-                                   const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
-                                   void* dv, void* workspace, size_t ws_bytes, void* stream) {
+                                   const int32_t* cu_seqlens, int32_t n_docs, int32_t window, void* dq,
+                                   void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
   CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(window >= 0, CP_ERR_INVALID_ARG, "window must be >= 0");
   CP_REQUIRE(P >= 1 && P <= 64, CP_ERR_INVALID_ARG, "P must be in [1, 64]");
   CP_REQUIRE(S >= 0, CP_ERR_INVALID_ARG, "S must be >= 0");
   CP_REQUIRE(Hq % P == 0, CP_ERR_SHAPE, "Ulysses needs Hq % P == 0");
@@ -1129,6 +1138,7 @@ cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, 
   a.scale = 1.0f / sqrtf((float)D);
   a.scale_log2 = a.scale * 1.4426950408889634f;
   a.causal = 1; a.cu_seqlens = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0;
+  a.window = window;
   a.err = device_error_word();
   cp_status stt = launch_bwd(a, *s, dtype, (int64_t)P * S, (int64_t)P * S, st);
   delete s;

@@ -143,8 +143,9 @@ struct QTile {
 
 struct KeyCtx {
   int64_t pk_lo, pk_hi;
-  int64_t en_lo;  // end of the document holding pk_lo
-  int causal, docs;
+  int64_t en_lo;   // end of the document holding pk_lo
+  int64_t win_hi;  // pk_hi + window - 1 (last query position any key sees), INT64_MAX without
+  int causal, docs, window;
   int G, hk;
 };
 
@@ -161,7 +162,7 @@ __device__ __forceinline__ void qiter_init(QIter& it, const KSeg* segs, int nseg
   it.hh = 0;
   it.si = 0;
   it.i = it.hi = 0;
-  if (nseg > 0) query_tile_range(segs[0], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
+  if (nseg > 0) query_tile_range(segs[0], kTileRows, c.pk_lo, c.causal, c.win_hi, it.i, it.hi);
 }
 
 __device__ __forceinline__ bool qiter_next(QIter& it, const KeyCtx& c, QTile& t) {
@@ -179,17 +180,18 @@ __device__ __forceinline__ bool qiter_next(QIter& it, const KeyCtx& c, QTile& t)
       t.h = c.hk * c.G + it.hh;
       t.full = (nq == kTileRows) && (c.causal ? pq_lo >= c.pk_hi : 1) && !c.docs;
       if (c.docs && c.causal) t.full = (nq == kTileRows) && pq_lo >= c.pk_hi && c.en_lo > pq_hi;
+      if (c.window > 0) t.full = t.full && pq_hi - c.pk_lo < c.window;
       ++it.i;
       return true;
     }
     if (it.si < it.nseg && ++it.si < it.nseg) {
-      query_tile_range(it.segs[it.si], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
+      query_tile_range(it.segs[it.si], kTileRows, c.pk_lo, c.causal, c.win_hi, it.i, it.hi);
       continue;
     }
     if (++it.hh < c.G) {
       it.si = 0;
       it.i = it.hi = 0;
-      if (it.nseg > 0) query_tile_range(it.segs[0], kTileRows, c.pk_lo, c.causal, it.i, it.hi);
+      if (it.nseg > 0) query_tile_range(it.segs[0], kTileRows, c.pk_lo, c.causal, c.win_hi, it.i, it.hi);
     }
   }
   return false;
@@ -199,7 +201,7 @@ __device__ __forceinline__ int count_qtiles(const KSeg* segs, int nseg, const Ke
   int n = 0;
   for (int si = 0; si < nseg; ++si) {
     int lo, hi;
-    query_tile_range(segs[si], kTileRows, c.pk_lo, c.causal, lo, hi);
+    query_tile_range(segs[si], kTileRows, c.pk_lo, c.causal, c.win_hi, lo, hi);
     n += hi - lo;
   }
   return n * c.G;
@@ -236,6 +238,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     int64_t st;
     doc_bounds(a.cu_seqlens, a.n_docs, c.pk_lo, &st, &c.en_lo);
   }
+  c.window = a.window;
+  c.win_hi = a.window > 0 ? c.pk_hi + a.window - 1 : INT64_MAX;
 
   // The group's query runs, read at every tile by every role: shared memory when they fit.
   const int nseg = seg_end - seg_begin;
@@ -429,8 +433,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
             lo = max(lo, d2 <= 0 ? (int64_t)0 : (d2 + t.qstride - 1) / t.qstride);
           }
         }
+        if (c.window > 0) {  // need pq <= pk + window - 1
+          const int64_t d3 = pk + c.window - 1 - t.pq_lo;
+          hi = min(hi, d3 < 0 ? (int64_t)-1 : d3 / t.qstride);
+        }
       }
-      const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
+      const int ilo = (int)min(lo, (int64_t)kTileRows), ihi = (int)max(hi, (int64_t)-1);
       if (!wait_all(&bars->q_full[st], (j / A_QST) & 1, abort_flag, a.err)) { ok = false; break; }
       const float* lse_st = lse_all + st * 2 * kTileRows + cb;
       const float* del_st = lse_st + kTileRows;
@@ -585,7 +593,8 @@ struct BBars {
 struct TileCtx {
   int64_t pq_lo, pq_hi;
   int64_t st_lo, st_hi, en_lo, en_hi;
-  int causal, docs;
+  int64_t win_lo;  // pq_lo - window + 1 (first key position any query sees), INT64_MIN without
+  int causal, docs, window;
 };
 
 struct KvTile {
@@ -604,7 +613,8 @@ struct KIter {
 };
 
 __device__ __forceinline__ void kiter_range(KIter& it, const TileCtx& c) {
-  key_tile_range(it.segs[it.si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, it.i, it.hi);
+  key_tile_range(it.segs[it.si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, c.win_lo, it.i,
+                 it.hi);
 }
 
 __device__ __forceinline__ void kiter_init(KIter& it, const KSeg* segs, int nseg, const TileCtx& c) {
@@ -628,7 +638,8 @@ __device__ __forceinline__ bool kiter_next(KIter& it, const TileCtx& c, KvTile& 
       t.pk_lo = pk_lo;
       t.kstride = sg.pos_stride;
       t.full = (nk == kTileRows) && (!c.causal || pk_hi <= c.pq_lo) &&
-               (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo));
+               (!c.docs || (pk_lo >= c.st_hi && pk_hi < c.en_lo)) &&
+               (c.window == 0 || c.pq_hi - pk_lo < c.window);
       ++it.i;
       return true;
     }
@@ -641,7 +652,7 @@ __device__ __forceinline__ int count_ktiles(const KSeg* segs, int nseg, const Ti
   int n = 0;
   for (int si = 0; si < nseg; ++si) {
     int lo, hi;
-    key_tile_range(segs[si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, lo, hi);
+    key_tile_range(segs[si], kTileRows, c.pq_hi, c.st_lo, c.en_hi, c.causal, c.docs, c.win_lo, lo, hi);
     n += hi - lo;
   }
   return n;
@@ -677,6 +688,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     doc_bounds(a.cu_seqlens, a.n_docs, c.pq_lo, &c.st_lo, &c.en_lo);
     doc_bounds(a.cu_seqlens, a.n_docs, c.pq_hi, &c.st_hi, &c.en_hi);
   }
+  c.window = a.window;
+  c.win_lo = a.window > 0 ? c.pq_lo - a.window + 1 : INT64_MIN;
 
   // The group's key runs, read at every tile by every role: shared memory when they fit.
   const int nseg = seg_end - seg_begin;
@@ -858,8 +871,12 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
           const int64_t db = en_r - 1 - t.pk_lo;
           hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
         }
+        if (c.window > 0) {  // need pk >= pq - window + 1
+          const int64_t dw = pq - c.window + 1 - t.pk_lo;
+          lo = max(lo, dw <= 0 ? (int64_t)0 : (dw + t.kstride - 1) / t.kstride);
+        }
       }
-      const int ilo = (int)lo, ihi = (int)max(hi, (int64_t)-1);
+      const int ilo = (int)min(lo, (int64_t)kTileRows), ihi = (int)max(hi, (int64_t)-1);
       // phase 1: P from S, then release S for the next tile
       if (!wait_all(&bars->s_full, j & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();

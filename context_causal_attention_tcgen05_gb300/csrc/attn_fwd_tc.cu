@@ -86,6 +86,8 @@ struct Bars {
 struct SpanCtx {
   int64_t pq_lo, pq_hi;                // positions of the first / last valid query rows
   int64_t st_lo, st_hi, en_lo, en_hi;  // document [start, end) of pq_lo and pq_hi
+  int64_t win_lo;                      // pq_lo - window + 1 (sliding window), INT64_MIN without
+  int32_t window;
 };
 
 struct KvTile {
@@ -99,6 +101,8 @@ __device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t
   c.pq_lo = pq_lo;
   c.pq_hi = pq_hi;
   c.st_lo = c.st_hi = c.en_lo = c.en_hi = 0;
+  c.window = a.window;
+  c.win_lo = a.window > 0 ? pq_lo - a.window + 1 : INT64_MIN;
   if (a.cu_seqlens) {
     doc_bounds(a.cu_seqlens, a.n_docs, pq_lo, &c.st_lo, &c.en_lo);
     doc_bounds(a.cu_seqlens, a.n_docs, pq_hi, &c.st_hi, &c.en_hi);
@@ -108,7 +112,7 @@ __device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t
 // Visible key/value tiles [lo, hi) of one segment for the CTA's query span.
 __device__ __forceinline__ void seg_range(const KSeg& sg, const SpanCtx& c, int causal, int docs,
                                           int& lo, int& hi) {
-  key_tile_range(sg, BN, c.pq_hi, c.st_lo, c.en_hi, causal, docs, lo, hi);
+  key_tile_range(sg, BN, c.pq_hi, c.st_lo, c.en_hi, causal, docs, c.win_lo, lo, hi);
 }
 
 // Walks the visible key/value tiles of the CTA's segments in order.  Identical in every role.
@@ -158,7 +162,8 @@ __device__ __forceinline__ int count_tiles(const KSeg* segs, int nseg, const Spa
 // Every (row, key) pair of the tile visible for this query span (no mask needed)?
 __device__ __forceinline__ bool tile_full(const SpanCtx& c, const KvTile& t, int causal, int docs) {
   return (t.nk == BN) && (!causal || t.pk_hi <= c.pq_lo) &&
-         (!docs || (t.pk_lo >= c.st_hi && t.pk_hi < c.en_lo));
+         (!docs || (t.pk_lo >= c.st_hi && t.pk_hi < c.en_lo)) &&
+         (c.window == 0 || c.pq_hi - t.pk_lo < c.window);
 }
 
 template <int D>
@@ -402,7 +407,11 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
             const int64_t db = en_r - 1 - t.pk_lo;
             hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
           }
-          ilo = (int)lo;
+          if (a.window > 0) {  // key within window - 1 positions before the query
+            const int64_t dw = pq - a.window + 1 - t.pk_lo;
+            lo = max(lo, dw <= 0 ? (int64_t)0 : (dw + t.kstride - 1) / t.kstride);
+          }
+          ilo = (int)min(lo, (int64_t)BN);
           ihi = (int)max(hi, (int64_t)-1);
         }
         if (!wwait(&bars->s_full[w], j & 1)) break;

@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
         if (i0 + row >= grp.nq) continue;  // warp-uniform
         bool vis = j < seg.nk;
         if (a.causal) vis = vis && (pk <= pq[r]);
+        if (a.window > 0) vis = vis && (pq[r] - pk < a.window);
         if (a.cu_seqlens) vis = vis && (pk >= dst[r]) && (pk < den[r]);
         float sc = -INFINITY;
         if (vis) {
@@ -224,6 +225,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(BwdArgs a, Schedule 
         if (a.cu_seqlens) doc_bounds(a.cu_seqlens, a.n_docs, pq, &dst, &den);
         bool vis = j < kg.nq;
         if (a.causal) vis = vis && (pk <= pq);
+        if (a.window > 0) vis = vis && (pq - pk < a.window);
         if (a.cu_seqlens) vis = vis && (pk >= dst) && (pk < den);
         const float lse = a.lse[(int64_t)h * a.lse_ld + qrow_idx];
         const float delta = a.delta[(int64_t)h * a.lse_ld + qrow_idx];

@@ -71,6 +71,7 @@ struct AttnArgs {
   int32_t* err;       // device error word
   int32_t total_units;
   int32_t o_f32;      // output dtype: 1 fp32, 0 same as input
+  int32_t window;     // sliding window (causal only): pos_q - pos_k < window; 0 = none
 };
 
 // Backward extras.
@@ -93,6 +94,7 @@ struct BwdArgs {
   int32_t n_docs;
   int32_t* err;
   int32_t total_units;
+  int32_t window;      // sliding window (causal only): pos_q - pos_k < window; 0 = none
 };
 
 // Device error codes written into the error word (first writer wins).
@@ -217,9 +219,11 @@ __device__ __forceinline__ void doc_bounds(const int32_t* cu, int32_t n_docs, in
 // Key tiles [lo, hi) of segment sg holding a key that some query of a span can
 // see: not after the span's last query pq_hi (causal), not at or after the end
 // en_hi of that query's document, not wholly before the start st_lo of the first
-// query's document (documents only).
+// query's document (documents only), not wholly before win_lo = (first query) -
+// window + 1 (sliding window; INT64_MIN without one).
 __device__ __forceinline__ void key_tile_range(const KSeg& sg, int tile, int64_t pq_hi, int64_t st_lo,
-                                               int64_t en_hi, int causal, int docs, int& lo, int& hi) {
+                                               int64_t en_hi, int causal, int docs, int64_t win_lo,
+                                               int& lo, int& hi) {
   const int64_t step = (int64_t)sg.pos_stride * tile;  // position advance per tile
   hi = (sg.nk + tile - 1) / tile;
   if (causal) {  // first key of the tile <= pq_hi
@@ -231,12 +235,13 @@ __device__ __forceinline__ void key_tile_range(const KSeg& sg, int tile, int64_t
     hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
   }
   lo = 0;
-  if (docs && hi > 0) {  // last key of the tile >= st_lo: a lower bound, then step forward
-    const int64_t d = st_lo - sg.pos_off;
+  const int64_t first = max(docs ? st_lo : INT64_MIN, win_lo);  // first position any query sees
+  if (first != INT64_MIN && hi > 0) {  // last key of the tile >= first: a lower bound, then step forward
+    const int64_t d = first - sg.pos_off;
     if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (d / sg.pos_stride - (tile - 1)) / tile));
     while (lo < hi) {
       const int n = min(tile, sg.nk - lo * tile);
-      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= st_lo) break;
+      if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= first) break;
       ++lo;
     }
   }
@@ -244,10 +249,15 @@ __device__ __forceinline__ void key_tile_range(const KSeg& sg, int tile, int64_t
 }
 
 // Query tiles [lo, hi) of segment sg holding a query at or after key position
-// pk_lo (causal); every tile otherwise.
+// pk_lo (causal; every tile otherwise) and starting no later than win_hi =
+// (last key) + window - 1 (sliding window; INT64_MAX without one).
 __device__ __forceinline__ void query_tile_range(const KSeg& sg, int tile, int64_t pk_lo, int causal,
-                                                 int& lo, int& hi) {
+                                                 int64_t win_hi, int& lo, int& hi) {
   hi = (sg.nk + tile - 1) / tile;
+  if (win_hi != INT64_MAX) {  // first query of the tile <= win_hi
+    const int64_t d = win_hi - sg.pos_off;
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / ((int64_t)sg.pos_stride * tile) + 1);
+  }
   lo = 0;
   if (causal) {  // last query of the tile >= pk_lo: a lower bound, then step forward
     const int64_t d = pk_lo - sg.pos_off;
@@ -258,6 +268,7 @@ __device__ __forceinline__ void query_tile_range(const KSeg& sg, int tile, int64
       ++lo;
     }
   }
+  if (lo > hi) lo = hi;
 }
 
 // Locates unit u in a schedule: query group, query tile index, head.

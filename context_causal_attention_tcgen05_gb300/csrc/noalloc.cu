@@ -78,9 +78,11 @@ extern "C" cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, con
   if (dtype == CP_BF16 && !(D == 64 || D == 128))
     return bad(CP_ERR_DTYPE, "bf16 attention supports D = 64 or 128");
   if (Sq < 0 || Sk < 0) return bad(CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
-  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0};
+  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0, 0};
   if (mask) m = *mask;
   if (m.q_stride < 1 || m.k_stride < 1) return bad(CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  if (m.window < 0) return bad(CP_ERR_INVALID_ARG, "mask window must be >= 0");
+  if (m.window > 0 && !m.causal) return bad(CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
   const int64_t qmax = m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0);
   const int64_t kmax = m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0);
   if (llabs(m.q_offset) > INT32_MAX || llabs(m.k_offset) > INT32_MAX || llabs(qmax) > INT32_MAX ||
@@ -150,6 +152,7 @@ extern "C" cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, con
   a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)Sq;
   a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
+  a.window = m.window;
   a.err = device_error_word();
   st = (is_bf16 && D == 128) ? launch_attn_bwd_tc(a, sched, Sq, Sk, s)
                              : launch_attn_bwd_simt(a, sched, is_bf16, s);

@@ -106,6 +106,7 @@ typedef struct {
   int64_t q_stride, k_stride;
   const int32_t* cu_seqlens;
   int32_t n_docs;
+  int32_t window;  /* sliding window: with causal, key visible iff pos_q - pos_k < window; 0 = none */
 } cp_mask;
 
 /* ---------------------------------------------------------------- block attention */
@@ -253,11 +254,13 @@ CP_API cp_status cp_ring_attention_bwd(const void* q, const void* k, const void*
  * key/value head is replicated P/Hkv times (the chapter's note on grouped
  * heads under Ulysses), so rank p reads head p / (P/Hkv), the head of its
  * query heads under the consecutive grouping.  Otherwise CP_ERR_SHAPE.
+ * `window` > 0 adds the sliding-window rule of cp_mask (the transformers pull
+ * request tests Ulysses with it); 0 = plain causal.  Negative: CP_ERR_INVALID_ARG.
  * out [S,Hq,D], lse [Hq,S].  workspace >= cp_workspace_size(CP_OP_ULYSSES_FWD). */
 CP_API cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,
                                int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
-                               const int32_t* cu_seqlens, int32_t n_docs, void* out, float* lse,
-                               void* workspace, size_t ws_bytes, void* stream);
+                               const int32_t* cu_seqlens, int32_t n_docs, int32_t window, void* out,
+                               float* lse, void* workspace, size_t ws_bytes, void* stream);
 
 /* Ulysses inside groups of P_ulysses ranks, the ring across P_ring groups (the
  * chapter's note that the two schemes compose: "Ulysses" splits the heads
@@ -292,8 +295,9 @@ CP_API cp_status cp_usp_attention(const void* q, const void* k, const void* v, i
 CP_API cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, const void* out,
                                           const float* lse, const void* dout, int64_t S, int32_t Hq,
                                           int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
-                                          const int32_t* cu_seqlens, int32_t n_docs, void* dq, void* dk,
-                                          void* dv, void* workspace, size_t ws_bytes, void* stream);
+                                          const int32_t* cu_seqlens, int32_t n_docs, int32_t window,
+                                          void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                          void* stream);
 
 /* Workspace bytes needed by `op` (a cp_op) for these sizes; `mode` is the
  * cp_ring_mode for CP_OP_RING_FWD and ignored otherwise.  For CP_OP_BLOCK_BWD

@@ -52,6 +52,12 @@ def test_block_fwd_refusals(lib):
     m = cpa.cp_mask()
     m.causal, m.q_stride, m.k_stride = 1, 0, 1
     assert _fwd(lib, mask=ctypes.byref(m)) == -1          # stride 0
+    m.q_stride, m.window = 1, -4
+    assert _fwd(lib, mask=ctypes.byref(m)) == -1          # negative window
+    m.causal, m.window = 0, 16
+    assert _fwd(lib, mask=ctypes.byref(m)) == -5          # a window needs the causal rule
+    assert "causal" in cpa.cp_last_error()
+    assert ctypes.sizeof(cpa.cp_mask) == 56               # the window fits the struct's padding
     assert _fwd(lib, Sq=0) == 0                           # empty is a no-op
 
 
@@ -78,7 +84,8 @@ def test_ring_refusals(lib):
 
 def test_ulysses_refusals(lib):
     f = lib.cp_ulysses_attention
-    base = [P16, P16, P16, 32768, 32, 8, 128, 1, 16, None, 0, P16, P16, P16, 1 << 40, None]
+    # q k v S Hq Hkv D dtype P cu n_docs window out lse ws ws_bytes stream
+    base = [P16, P16, P16, 32768, 32, 8, 128, 1, 16, None, 0, 0, P16, P16, P16, 1 << 40, None]
     a = list(base)
     a[5] = 6
     st = f(*a)  # Hkv=6, P=16: neither a divisor nor a multiple of the key/value heads
@@ -88,8 +95,11 @@ def test_ulysses_refusals(lib):
     a[3] = 32769
     assert f(*a) == -2                                    # S % P
     a = list(base)  # Hkv=8 < P=16 is accepted (heads replicated): it reaches the workspace check
-    a[14] = 100
+    a[15] = 100
     assert f(*a) == -6
+    a = list(base)
+    a[11] = -1                                            # negative window
+    assert f(*a) == -1
     need = ctypes.c_size_t()
     assert lib.cp_workspace_size(2, 32768, 32, 8, 128, 1, 16, 0, ctypes.byref(need)) == 0
     need_plain = ctypes.c_size_t()
@@ -119,8 +129,8 @@ def test_usp_refusals(lib):
 
 def test_ulysses_bwd_refusals(lib):
     f = lib.cp_ulysses_attention_bwd
-    # q k v out lse dout S Hq Hkv D dtype P cu n_docs dq dk dv ws ws_bytes stream
-    base = [P16, P16, P16, P16, P16, P16, 4096, 32, 8, 128, 1, 16, None, 0, P16, P16, P16, P16, 1 << 40, None]
+    # q k v out lse dout S Hq Hkv D dtype P cu n_docs window dq dk dv ws ws_bytes stream
+    base = [P16, P16, P16, P16, P16, P16, 4096, 32, 8, 128, 1, 16, None, 0, 0, P16, P16, P16, P16, 1 << 40, None]
     a = list(base)
     a[8] = 6
     assert f(*a) == -2 and "Hkv" in cpa.cp_last_error()
@@ -128,7 +138,7 @@ def test_ulysses_bwd_refusals(lib):
     a[7] = 24                                             # Hq % P
     assert f(*a) == -2
     a = list(base)
-    a[18] = 100                                           # workspace too small
+    a[19] = 100                                           # workspace too small
     assert f(*a) == -6
     a = list(base)
     a[4] = None                                           # lse required

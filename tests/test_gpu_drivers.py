@@ -160,6 +160,24 @@ def test_usp_bf16_medium(Pu, Pr, layout, Hkv, docs):
     check_ok()
 
 
+@pytest.mark.parametrize("Hq,Hkv,P,W,docs", [(8, 4, 4, 100, False), (8, 2, 4, 300, True), (8, 8, 8, 1, False)])
+def test_ulysses_window_fwd_bwd(Hq, Hkv, P, W, docs):
+    # the sliding-window rule through the Ulysses drivers (forward and backward)
+    S, D = 512, 128
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=19, with_dout=True)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 300, seed=6)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu, window=W)
+    o, l = cpa.cp_ulysses_attention(q.cuda(), k.cuda(), v.cuda(), P, cu_seqlens=cu_d, window=W)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"ulysses window {W}")
+    dq, dk, dv = cpa.cp_ulysses_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P,
+                                              cu_seqlens=cu_d, window=W)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu, window=W)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+    check_ok()
+
+
 @pytest.mark.parametrize("layout,docs", [("zigzag", False), ("contiguous", False), ("striped", False),
                                          ("zigzag", True), ("striped", True)])
 def test_ring_bwd_bf16_medium(layout, docs):

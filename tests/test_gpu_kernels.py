@@ -130,6 +130,55 @@ def test_block_fwd(dtype, case):
     check_ok()
 
 
+WINDOW_CASES = [
+    # Sq, Sk, Hq, Hkv, D, q_off, k_off, window, docs
+    (300, 300, 4, 2, 128, 0, 0, 64, None),            # window inside a 128-key tile
+    (300, 300, 4, 2, 128, 0, 0, 1, None),             # each query sees only itself
+    (520, 520, 2, 1, 128, 0, 0, 200, None),           # window spanning tiles, ragged tail
+    (256, 256, 4, 2, 128, 0, 0, 100, [50, 1, 77, 128]),   # window and packed documents
+    (200, 300, 2, 2, 64, 150, 0, 90, None),           # later queries against an earlier block
+    (129, 129, 4, 4, 128, 0, 0, 129, None),           # window covering the whole block
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("case", WINDOW_CASES)
+def test_block_fwd_window(dtype, case):
+    Sq, Sk, Hq, Hkv, D, qo, ko, W, docs = case
+    g = torch.Generator().manual_seed(33)
+    q = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    k = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    ref_o, ref_l = oracle.attention(q, k, v, True, qo, ko, cu_seqlens=cu, window=W)
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, 1, 1, cu_d, window=W)
+    assert_close(o, l, ref_o, ref_l, dtype, str(case))
+    check_ok()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("case", WINDOW_CASES[:4])
+def test_block_bwd_window(dtype, case):
+    Sq, Sk, Hq, Hkv, D, qo, ko, W, docs = case
+    g = torch.Generator().manual_seed(43)
+    q = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    k = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(Sk, Hkv, D, generator=g).to(dtype)
+    do = torch.randn(Sq, Hq, D, generator=g).to(dtype)
+    cu = None if docs is None else cu_seqlens_from_lengths(docs)
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, 1, 1, cu_d, window=W)
+    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, True, qo, ko, 1, 1, cu_d,
+                                       window=W)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, qo, ko, cu_seqlens=cu, window=W)
+    tol = TOL_OUT[dtype] if dtype == torch.float32 else 2e-2
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = max_err(got, ref)
+        assert e <= tol * max(1.0, float(np.abs(ref).max())), f"{name} {case}: {e}"
+    check_ok()
+
+
 # ---------------------------------------------------------------- block attention backward
 
 BWD_CASES = [
