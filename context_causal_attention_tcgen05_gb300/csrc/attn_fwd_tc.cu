@@ -86,8 +86,8 @@ struct Bars {
 struct SpanCtx {
   int64_t pq_lo, pq_hi;                // positions of the first / last valid query rows
   int64_t st_lo, st_hi, en_lo, en_hi;  // document [start, end) of pq_lo and pq_hi
-  int64_t win_lo;                      // pq_lo - window + 1 (sliding window), INT64_MIN without
-  int32_t window;
+  int64_t win_lo;   // pq_lo - window + 1: first position any row's window reaches (INT64_MIN: none)
+  int64_t full_lo;  // first key position every row of the span sees (document and window starts)
 };
 
 struct KvTile {
@@ -97,15 +97,17 @@ struct KvTile {
   int32_t kstride;
 };
 
-__device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int64_t pq_lo, int64_t pq_hi) {
+__device__ __forceinline__ void span_init(SpanCtx& c, const AttnArgs& a, int32_t window, int64_t pq_lo,
+                                          int64_t pq_hi) {
   c.pq_lo = pq_lo;
   c.pq_hi = pq_hi;
   c.st_lo = c.st_hi = c.en_lo = c.en_hi = 0;
-  c.window = a.window;
-  c.win_lo = a.window > 0 ? pq_lo - a.window + 1 : INT64_MIN;
+  c.win_lo = window > 0 ? pq_lo - window + 1 : INT64_MIN;
+  c.full_lo = window > 0 ? pq_hi - window + 1 : INT64_MIN;
   if (a.cu_seqlens) {
     doc_bounds(a.cu_seqlens, a.n_docs, pq_lo, &c.st_lo, &c.en_lo);
     doc_bounds(a.cu_seqlens, a.n_docs, pq_hi, &c.st_hi, &c.en_hi);
+    c.full_lo = max(c.full_lo, c.st_hi);
   }
 }
 
@@ -161,9 +163,8 @@ __device__ __forceinline__ int count_tiles(const KSeg* segs, int nseg, const Spa
 
 // Every (row, key) pair of the tile visible for this query span (no mask needed)?
 __device__ __forceinline__ bool tile_full(const SpanCtx& c, const KvTile& t, int causal, int docs) {
-  return (t.nk == BN) && (!causal || t.pk_hi <= c.pq_lo) &&
-         (!docs || (t.pk_lo >= c.st_hi && t.pk_hi < c.en_lo)) &&
-         (c.window == 0 || c.pq_hi - t.pk_lo < c.window);
+  return (t.nk == BN) && (!causal || t.pk_hi <= c.pq_lo) && t.pk_lo >= c.full_lo &&
+         (!docs || t.pk_hi < c.en_lo);
 }
 
 template <int D>
@@ -178,7 +179,9 @@ __device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
   return ptx::smem_desc_sw128(tile_base + kk * (16 * 128), 128 * 128, 1024);
 }
 
-template <int D, bool kOutF32>
+// kWin: the sliding window is applied (a.window > 0); without it the window
+// terms fold away at compile time.
+template <int D, bool kOutF32, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Schedule s,
                    const __grid_constant__ CUtensorMap tm_q,
@@ -195,6 +198,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   int g, tile, h;
   decode_unit(s, kRowsPerCta, a.Hq, blockIdx.x, &g, &tile, &h);
   const int hk = h / (a.Hq / a.Hkv);
+  const int32_t window = kWin ? a.window : 0;
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
   const int32_t qpos_off = s.g[g].pos_off, qpos_st = s.g[g].pos_stride;
   const int seg_begin = s.g[g].seg_begin, seg_end = seg_begin + s.g[g].seg_count;
@@ -207,7 +211,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   SpanCtx cta;  // both query tiles together
   {
     const int64_t lo = (int64_t)qpos_off + (int64_t)qpos_st * i0;
-    span_init(cta, a, lo, lo + (int64_t)qpos_st * (nq0 + nq1 - 1));
+    span_init(cta, a, window, lo, lo + (int64_t)qpos_st * (nq0 + nq1 - 1));
   }
 
   // The group's segments, read at every tile by every role: shared memory when they fit.
@@ -377,10 +381,12 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
     if (w == 0 || has1) {
       SpanCtx mine;
       const int64_t pq_lo_w = cta.pq_lo + (int64_t)qpos_st * (w * BM);
-      span_init(mine, a, pq_lo_w, pq_lo_w + (int64_t)qpos_st * (nq_w - 1));
+      span_init(mine, a, window, pq_lo_w, pq_lo_w + (int64_t)qpos_st * (nq_w - 1));
       const int64_t pq = pq_lo_w + (int64_t)qpos_st * r;
       int64_t st_r = 0, en_r = 0;
       if (docs && r < nq_w) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
+      // first key position the row sees: its document's start and its window's start
+      const int64_t first_r = max(docs ? st_r : INT64_MIN, window > 0 ? pq - window + 1 : INT64_MIN);
       const float sl2 = a.scale_log2;
       const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       float m = -INFINITY, l = 0.f;
@@ -402,15 +408,11 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
             hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
           }
           if (docs) {
-            const int64_t da = st_r - t.pk_lo;
-            lo = max(lo, da <= 0 ? (int64_t)0 : (da + t.kstride - 1) / t.kstride);
             const int64_t db = en_r - 1 - t.pk_lo;
             hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
           }
-          if (a.window > 0) {  // key within window - 1 positions before the query
-            const int64_t dw = pq - a.window + 1 - t.pk_lo;
-            lo = max(lo, dw <= 0 ? (int64_t)0 : (dw + t.kstride - 1) / t.kstride);
-          }
+          if (first_r > t.pk_lo)  // keys before first_r are hidden
+            lo = (first_r - t.pk_lo + t.kstride - 1) / t.kstride;
           ilo = (int)min(lo, (int64_t)BN);
           ihi = (int)max(hi, (int64_t)-1);
         }
@@ -593,11 +595,11 @@ cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols)
   return CP_OK;
 }
 
-template <int D, bool kOutF32>
+template <int D, bool kOutF32, bool kWin>
 cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, int64_t units, cudaStream_t st) {
   using L = Layout<D>;
-  auto kern = attn_fwd_tc_kernel<D, kOutF32>;
+  auto kern = attn_fwd_tc_kernel<D, kOutF32, kWin>;
   // setmaxnreg.inc waits until the registers it asks for are free in the block's
   // launch budget, so launch only if the split fits that budget.
   cudaFuncAttributes fa;
@@ -629,12 +631,21 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
   if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * a.D)) != CP_OK) return r;
   if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;
   if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;
-  if (a.D == 128)
-    return a.o_f32 ? launch_typed<128, true>(a, s, mq, mk, mv, units, st)
-                   : launch_typed<128, false>(a, s, mq, mk, mv, units, st);
-  if (a.D == 64)
-    return a.o_f32 ? launch_typed<64, true>(a, s, mq, mk, mv, units, st)
-                   : launch_typed<64, false>(a, s, mq, mk, mv, units, st);
+  const bool win = a.window > 0;
+  if (a.D == 128) {
+    if (win)
+      return a.o_f32 ? launch_typed<128, true, true>(a, s, mq, mk, mv, units, st)
+                     : launch_typed<128, false, true>(a, s, mq, mk, mv, units, st);
+    return a.o_f32 ? launch_typed<128, true, false>(a, s, mq, mk, mv, units, st)
+                   : launch_typed<128, false, false>(a, s, mq, mk, mv, units, st);
+  }
+  if (a.D == 64) {
+    if (win)
+      return a.o_f32 ? launch_typed<64, true, true>(a, s, mq, mk, mv, units, st)
+                     : launch_typed<64, false, true>(a, s, mq, mk, mv, units, st);
+    return a.o_f32 ? launch_typed<64, true, false>(a, s, mq, mk, mv, units, st)
+                   : launch_typed<64, false, false>(a, s, mq, mk, mv, units, st);
+  }
   set_last_error("tcgen05 attention supports D = 64 or 128");
   return CP_ERR_UNSUPPORTED;
 }
