@@ -207,6 +207,9 @@ __device__ __forceinline__ int count_qtiles(const KSeg* segs, int nseg, const Ke
   return n * c.G;
 }
 
+// kWin: the sliding window is applied (a.window > 0); without it the window
+// terms fold away at compile time.  Same flag on the dQ kernel.
+template <bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Schedule s,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -238,8 +241,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     int64_t st;
     doc_bounds(a.cu_seqlens, a.n_docs, c.pk_lo, &st, &c.en_lo);
   }
-  c.window = a.window;
-  c.win_hi = a.window > 0 ? c.pk_hi + a.window - 1 : INT64_MAX;
+  c.window = kWin ? a.window : 0;
+  c.win_hi = c.window > 0 ? c.pk_hi + c.window - 1 : INT64_MAX;
 
   // The group's query runs, read at every tile by every role: shared memory when they fit.
   const int nseg = seg_end - seg_begin;
@@ -658,6 +661,7 @@ __device__ __forceinline__ int count_ktiles(const KSeg* segs, int nseg, const Ti
   return n;
 }
 
+template <bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Schedule s,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -688,8 +692,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     doc_bounds(a.cu_seqlens, a.n_docs, c.pq_lo, &c.st_lo, &c.en_lo);
     doc_bounds(a.cu_seqlens, a.n_docs, c.pq_hi, &c.st_hi, &c.en_hi);
   }
-  c.window = a.window;
-  c.win_lo = a.window > 0 ? c.pq_lo - a.window + 1 : INT64_MIN;
+  c.window = kWin ? a.window : 0;
+  c.win_lo = c.window > 0 ? c.pq_lo - c.window + 1 : INT64_MIN;
 
   // The group's key runs, read at every tile by every role: shared memory when they fit.
   const int nseg = seg_end - seg_begin;
@@ -1084,7 +1088,10 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   }
   // setmaxnreg.inc waits until the registers it asks for are free in the block's launch
   // budget, so launch only if each kernel's compiled register count covers the split.
-  for (const void* kfn : {(const void*)attn_bwd_dkdv_kernel, (const void*)attn_bwd_dq_kernel}) {
+  const bool win = a.window > 0;
+  auto dkdv_kernel = win ? attn_bwd_dkdv_kernel<true> : attn_bwd_dkdv_kernel<false>;
+  auto dq_kernel = win ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
+  for (const void* kfn : {(const void*)dkdv_kernel, (const void*)dq_kernel}) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kfn);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncGetAttributes(attn_bwd)");
@@ -1104,10 +1111,10 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   // dK / dV over the key-major schedule
   int64_t units = schedule_units(s, kTileRows, a.Hkv);
   if (units > 0) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          ALayout::kSmemRequest);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dkdv)");
-    attn_bwd_dkdv_kernel<<<(unsigned)units, kThreads, ALayout::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
+    dkdv_kernel<<<(unsigned)units, kThreads, ALayout::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
     if ((r = cuda_check(cudaGetLastError(), "attn_bwd_dkdv_kernel launch")) != CP_OK) return r;
   }
   // dQ over the query-major schedule (same pairs)
@@ -1119,13 +1126,13 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   }
   units = schedule_units(*qm, kTileRows, a.Hq);
   if (units > 0) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          BLayout::kSmemRequest);
     if (e != cudaSuccess) {
       delete qm;
       return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dq)");
     }
-    attn_bwd_dq_kernel<<<(unsigned)units, kThreads, BLayout::kSmemRequest, st>>>(a, *qm, mk, mv);
+    dq_kernel<<<(unsigned)units, kThreads, BLayout::kSmemRequest, st>>>(a, *qm, mk, mv);
     r = cuda_check(cudaGetLastError(), "attn_bwd_dq_kernel launch");
   }
   delete qm;
