@@ -58,7 +58,66 @@ int64_t schedule_units(Schedule& s, int tile_rows, int heads) {
     s.g[i].tile0 = (int32_t)tiles;
     tiles += (s.g[i].nq + tile_rows - 1) / tile_rows;
   }
+  s.n_order = 0;
   return tiles * heads;
+}
+
+// Tiles of segment sg (tiles of `tile` rows) that a tile of the group spanning
+// positions [p_lo, p_hi] works on: query-major, key tiles not after p_hi and not
+// wholly before the window start; key-major, query tiles not wholly before p_lo
+// and starting within p_hi + window - 1.
+static int64_t tiles_seen(const KSeg& sg, int tile, int64_t p_lo, int64_t p_hi, bool key_major,
+                          int causal, int window) {
+  const int64_t n = (sg.nk + tile - 1) / tile;
+  const int64_t step = (int64_t)sg.pos_stride * tile;
+  int64_t lo = 0, hi = n;
+  auto clamp = [&](int64_t x) { return x < 0 ? (int64_t)0 : (x > n ? n : x); };
+  if (!key_major) {
+    if (causal) hi = clamp(p_hi < sg.pos_off ? 0 : (p_hi - sg.pos_off) / step + 1);
+    if (window > 0) {  // last key of tile i >= p_lo - window + 1
+      const int64_t first = p_lo - window + 1 - sg.pos_off;
+      if (first > 0) lo = clamp((first / sg.pos_stride - (tile - 1)) / tile);
+    }
+  } else {
+    if (causal) {  // last query of tile i >= p_lo
+      const int64_t d = p_lo - sg.pos_off;
+      if (d > 0) lo = clamp((d / sg.pos_stride - (tile - 1)) / tile);
+    }
+    if (window > 0) {  // first query of tile i <= p_hi + window - 1
+      const int64_t last = p_hi + window - 1 - sg.pos_off;
+      hi = clamp(last < 0 ? 0 : last / step + 1);
+    }
+  }
+  return hi > lo ? hi - lo : 0;
+}
+
+void schedule_order(Schedule& s, int tile_rows, int other_tile, bool key_major, int causal, int window,
+                    bool docs) {
+  s.n_order = 0;
+  if (docs || (!causal && window <= 0)) return;
+  std::vector<std::pair<int64_t, int32_t>> w;  // (weight, entry) in the default order
+  for (int gi = 0; gi < s.n_groups; ++gi) {
+    const QGroup& g = s.g[gi];
+    const int ntiles = (g.nq + tile_rows - 1) / tile_rows;
+    if (ntiles >= (1 << 20)) return;
+    for (int local = 0; local < ntiles; ++local) {
+      const int t = ntiles - 1 - local;
+      const int64_t r0 = (int64_t)t * tile_rows, r1 = std::min<int64_t>(r0 + tile_rows, g.nq) - 1;
+      const int64_t p_lo = g.pos_off + (int64_t)g.pos_stride * r0;
+      const int64_t p_hi = g.pos_off + (int64_t)g.pos_stride * r1;
+      int64_t seen = 0;
+      for (int si = g.seg_begin; si < g.seg_begin + g.seg_count; ++si)
+        seen += tiles_seen(s.s[si], other_tile, p_lo, p_hi, key_major, causal, window);
+      w.emplace_back(seen, (int32_t)((gi << 20) | t));
+      if ((int)w.size() > kMaxOrder) return;
+    }
+  }
+  std::stable_sort(w.begin(), w.end(),
+                   [](const std::pair<int64_t, int32_t>& x, const std::pair<int64_t, int32_t>& y) {
+                     return x.first > y.first;
+                   });
+  for (size_t i = 0; i < w.size(); ++i) s.order[i] = w[i].second;
+  s.n_order = (int32_t)w.size();
 }
 
 }  // namespace cpa

@@ -1110,6 +1110,7 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
 
   // dK / dV over the key-major schedule
   int64_t units = schedule_units(s, kTileRows, a.Hkv);
+  schedule_order(s, kTileRows, kTileRows, true, a.causal, a.window, a.cu_seqlens != nullptr);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          ALayout::kSmemRequest);
@@ -1125,6 +1126,7 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
     return CP_ERR_UNSUPPORTED;
   }
   units = schedule_units(*qm, kTileRows, a.Hq);
+  schedule_order(*qm, kTileRows, kTileRows, false, a.causal, a.window, a.cu_seqlens != nullptr);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          BLayout::kSmemRequest);

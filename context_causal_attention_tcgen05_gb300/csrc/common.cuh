@@ -20,6 +20,7 @@ namespace cpa {
 
 constexpr int kMaxGroups = 64;
 constexpr int kMaxSegs = 1024;
+constexpr int kMaxOrder = 2048;  // (group, tile) pairs a launch order table can hold
 
 // A run of query rows that share one affine position map.
 struct QGroup {
@@ -49,6 +50,10 @@ struct Schedule {
   int32_t n_segs;
   QGroup g[kMaxGroups];
   KSeg s[kMaxSegs];
+  // Launch order of the (group, tile) pairs, heaviest first: entry = group << 20 | tile.
+  // n_order = 0: groups in order, each group's tiles last to first.
+  int32_t n_order;
+  int32_t order[kMaxOrder];
 };
 
 // Everything else an attention launch needs (pointers, strides, mask).
@@ -152,7 +157,18 @@ enum GatherKind : int {
 };
 
 // Fills group tile prefix sums for a query tile height; returns total units (tiles x heads).
+// Clears the launch order table.
 int64_t schedule_units(Schedule& s, int tile_rows, int heads);
+
+// Fills the launch order table (after schedule_units with the same tile_rows) so that
+// the CTAs with the most visible tiles of the other side start first and the lightest
+// fill the last wave (the backward kernels use it; the forward's own order measured as
+// fast).  The weight counts tiles from positions alone (causal rule and
+// sliding window); with documents, without the causal rule, or when the pairs do not
+// fit the table, the order is left as schedule_units set it.  key_major: groups are
+// key runs and segments query runs (the key-stationary backward).
+void schedule_order(Schedule& s, int tile_rows, int other_tile, bool key_major, int causal,
+                    int window, bool docs);
 
 }  // namespace cpa
 
@@ -276,6 +292,13 @@ __device__ __forceinline__ void decode_unit(const Schedule& s, int tile_rows, in
                                             int* g_out, int* tile_out, int* h_out) {
   int h = u % heads;
   int rest = u / heads;
+  if (s.n_order > 0) {
+    const int e = s.order[rest];
+    *g_out = e >> 20;
+    *tile_out = e & 0xfffff;
+    *h_out = h;
+    return;
+  }
   int g = 0;
   for (int i = 1; i < s.n_groups; ++i)
     if (s.g[i].tile0 <= rest) g = i;
