@@ -426,19 +426,19 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       } else if (!t.full) {
         if (c.causal) {
           const int64_t d0 = pk - t.pq_lo;  // need pq >= pk
-          lo = max(lo, d0 <= 0 ? (int64_t)0 : (d0 + t.qstride - 1) / t.qstride);
+          lo = max(lo, d0 <= 0 ? (int64_t)0 : udiv_pos(d0 + t.qstride - 1, t.qstride));
         }
         if (c.docs) {
           const int64_t d1 = en_k - 1 - t.pq_lo;  // need pq < end of the key's document
-          hi = min(hi, d1 < 0 ? (int64_t)-1 : d1 / t.qstride);
+          hi = min(hi, d1 < 0 ? (int64_t)-1 : udiv_pos(d1, t.qstride));
           if (!c.causal) {  // and pq >= start of the key's document
             const int64_t d2 = st_k - t.pq_lo;
-            lo = max(lo, d2 <= 0 ? (int64_t)0 : (d2 + t.qstride - 1) / t.qstride);
+            lo = max(lo, d2 <= 0 ? (int64_t)0 : udiv_pos(d2 + t.qstride - 1, t.qstride));
           }
         }
         if (c.window > 0) {  // need pq <= pk + window - 1
           const int64_t d3 = pk + c.window - 1 - t.pq_lo;
-          hi = min(hi, d3 < 0 ? (int64_t)-1 : d3 / t.qstride);
+          hi = min(hi, d3 < 0 ? (int64_t)-1 : udiv_pos(d3, t.qstride));
         }
       }
       const int ilo = (int)min(lo, (int64_t)kTileRows), ihi = (int)max(hi, (int64_t)-1);
@@ -867,17 +867,17 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       } else if (!t.full) {
         if (c.causal) {
           const int64_t d = pq - t.pk_lo;
-          hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
+          hi = min(hi, d < 0 ? (int64_t)-1 : udiv_pos(d, t.kstride));
         }
         if (c.docs) {
           const int64_t da = st_r - t.pk_lo;
-          lo = max(lo, da <= 0 ? (int64_t)0 : (da + t.kstride - 1) / t.kstride);
+          lo = max(lo, da <= 0 ? (int64_t)0 : udiv_pos(da + t.kstride - 1, t.kstride));
           const int64_t db = en_r - 1 - t.pk_lo;
-          hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
+          hi = min(hi, db < 0 ? (int64_t)-1 : udiv_pos(db, t.kstride));
         }
         if (c.window > 0) {  // need pk >= pq - window + 1
           const int64_t dw = pq - c.window + 1 - t.pk_lo;
-          lo = max(lo, dw <= 0 ? (int64_t)0 : (dw + t.kstride - 1) / t.kstride);
+          lo = max(lo, dw <= 0 ? (int64_t)0 : udiv_pos(dw + t.kstride - 1, t.kstride));
         }
       }
       const int ilo = (int)min(lo, (int64_t)kTileRows), ihi = (int)max(hi, (int64_t)-1);

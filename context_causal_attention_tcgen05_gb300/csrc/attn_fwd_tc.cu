@@ -34,6 +34,9 @@
 // expiry the CTA records CP_ERR_DEVICE_TIMEOUT in the device error word,
 // drains its own copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
+#include <string.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -150,17 +153,6 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const SpanCtx& c, int ca
   return false;
 }
 
-__device__ __forceinline__ int count_tiles(const KSeg* segs, int nseg, const SpanCtx& c, int causal,
-                                           int docs) {
-  int n = 0;
-  for (int si = 0; si < nseg; ++si) {
-    int lo, hi;
-    seg_range(segs[si], c, causal, docs, lo, hi);
-    n += hi - lo;
-  }
-  return n;
-}
-
 // Every (row, key) pair of the tile visible for this query span (no mask needed)?
 __device__ __forceinline__ bool tile_full(const SpanCtx& c, const KvTile& t, int causal, int docs) {
   return (t.nk == BN) && (!causal || t.pk_hi <= c.pq_lo) && t.pk_lo >= c.full_lo &&
@@ -186,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Schedule s,
                    const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v) {
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -220,6 +213,21 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   const KSeg* segs = nseg <= kSegCap ? seg_sm : &s.s[seg_begin];
   if (nseg <= kSegCap)
     for (int i = threadIdx.x; i < nseg; i += kThreads) seg_sm[i] = s.s[seg_begin + i];
+  int pj = 0;
+  int issued[2] = {0, 0};
+  auto issue_kv = [&](const KvTile& t) {
+    const int st = pj & 1;
+    ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::kTile);
+#pragma unroll
+    for (int r = 0; r < D / 64; ++r) {
+      ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
+                       hk * D + r * 64, t.k_row);
+      ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
+                       hk * D + r * 64, t.k_row);
+    }
+    issued[st] = pj + 1;
+    ++pj;
+  };
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -232,14 +240,15 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
-    ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
-  }
   if (warp == kProducerWarp && lane == 0) {
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
+    if (!kOutF32 && a.o_tma) ptx::prefetch_tensormap(&tm_o);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(&bars->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -257,26 +266,14 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
         for (int r = 0; r < D / 64; ++r)
           ptx::tma_load_2d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
                            h * D + r * 64, q_row0 + i0 + w * BM);
-      TileIter it;
-      iter_init(it, segs, nseg, cta, causal, docs);
-      int j = 0;
+      TileIter pit;
+      iter_init(pit, segs, nseg, cta, causal, docs);
       KvTile t;
-      int issued[2] = {0, 0};
-      while (!*abort_flag && iter_next(it, cta, causal, docs, t)) {
-        const int st = j & 1;
-        if (j >= 2 && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j >> 1) - 1) & 1, abort_flag,
-                                              a.err, kWaitNs))
+      while (!*abort_flag && iter_next(pit, cta, causal, docs, t)) {
+        if (pj >= 2 && !ptx::mbar_wait_bounded(&bars->kv_empty[pj & 1], ((pj >> 1) - 1) & 1, abort_flag,
+                                               a.err, kWaitNs))
           break;
-        ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::kTile);
-#pragma unroll
-        for (int r = 0; r < D / 64; ++r) {
-          ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
-                           hk * D + r * 64, t.k_row);
-          ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
-                           hk * D + r * 64, t.k_row);
-        }
-        issued[st] = j + 1;
-        ++j;
+        issue_kv(t);
       }
       if (*abort_flag) {
         // drain: wait (bounded) for this CTA's own copies still in flight
@@ -290,6 +287,14 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // The tile count up front, one segment per lane.
+    int n_tiles = 0;
+    for (int si = lane; si < nseg; si += 32) {
+      int lo, hi;
+      seg_range(segs[si], cta, causal, docs, lo, hi);
+      n_tiles += hi - lo;
+    }
+    n_tiles = __reduce_add_sync(0xffffffffu, n_tiles);
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, 0, 1);  // V is MN-major
@@ -314,7 +319,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       // The issuing thread stalls at each tcgen05.mma until the pipe accepts it, so
       // every gap between two products holds at most one barrier wait and no
       // schedule walking (the tile count is known up front).
-      const int n = count_tiles(segs, nseg, cta, causal, docs);
+      const int n = n_tiles;
       bool ok = wait(&bars->q_full, 0);
       bool any = false;
       if (ok && n > 0) {
@@ -405,14 +410,14 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
           int64_t hi = t.nk - 1, lo = 0;
           if (causal) {
             const int64_t d = pq - t.pk_lo;
-            hi = min(hi, d < 0 ? (int64_t)-1 : d / t.kstride);
+            hi = min(hi, d < 0 ? (int64_t)-1 : udiv_pos(d, t.kstride));
           }
           if (docs) {
             const int64_t db = en_r - 1 - t.pk_lo;
-            hi = min(hi, db < 0 ? (int64_t)-1 : db / t.kstride);
+            hi = min(hi, db < 0 ? (int64_t)-1 : udiv_pos(db, t.kstride));
           }
           if (first_r > t.pk_lo)  // keys before first_r are hidden
-            lo = (first_r - t.pk_lo + t.kstride - 1) / t.kstride;
+            lo = udiv_pos(first_r - t.pk_lo + t.kstride - 1, t.kstride);
           ilo = (int)min(lo, (int64_t)BN);
           ihi = (int)max(hi, (int64_t)-1);
         }
@@ -500,8 +505,48 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
         const bool valid = r < nq_w;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const int64_t orow = (int64_t)(s.g[g].o_row0 + i0 + w * BM + r) * a.o_ld + (int64_t)h * D;
+        // bf16 output of a warp whose 32 rows are all valid: staged in this query tile's
+        // Q buffer (free once o_done fired) in the 128-byte swizzled layout of the O
+        // tensor map, then written by one TMA store per 64 columns.
+        const bool staged = !kOutF32 && a.o_tma && quad * 32 + 32 <= nq_w;
+        if (staged) {
+          uint8_t* stg = smem + L::kQ + w * L::kTile + quad * (32 * D * 2);
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t rr[32];
+            if (j > 0) {
+              ptx::tmem_ld32(lane_addr + 128 + ch * 32, rr);
+              ptx::tmem_wait_ld_regs(rr);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = 0u;
+            }
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int c = ch * 4 + v4;  // 16-byte chunk of the row (8 columns)
+              uint4* dst = reinterpret_cast<uint4*>(stg + (c >> 3) * 4096 + lane * 128 +
+                                                    (((c & 7) ^ (lane & 7)) << 4));
+              *dst = make_uint4(ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 0]) * inv_l,
+                                                 __uint_as_float(rr[8 * v4 + 1]) * inv_l),
+                                ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 2]) * inv_l,
+                                                 __uint_as_float(rr[8 * v4 + 3]) * inv_l),
+                                ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 4]) * inv_l,
+                                                 __uint_as_float(rr[8 * v4 + 5]) * inv_l),
+                                ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 6]) * inv_l,
+                                                 __uint_as_float(rr[8 * v4 + 7]) * inv_l));
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int32_t y0 = s.g[g].o_row0 + i0 + w * BM + quad * 32;
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) ptx::tma_store_2d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0);
+            ptx::bulk_commit_group();
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < D / 32 && !staged; ++ch) {
           uint32_t rr[32];
           if (j > 0) {
             ptx::tmem_ld32(lane_addr + 128 + ch * 32, rr);
@@ -540,6 +585,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
           const float Lr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
           a.lse[(int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + w * BM + r] = Lr;
         }
+        if (staged && lane == 0) ptx::bulk_wait_group_read0();  // the CTA's smem outlives the reads
       }
     }
     ptx::tc_fence_before();
@@ -575,21 +621,22 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D map over a [rows, H*D] bf16 buffer; box 64 columns x 128 rows, 128-byte swizzle.
-cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows = 128,
+                   bool report = true) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) {
-    set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
+    if (report) set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
     return CP_ERR_CUDA;
   }
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    set_last_error("cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
+    if (report) set_last_error("cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")");
     return CP_ERR_CUDA;
   }
   return CP_OK;
@@ -597,7 +644,7 @@ cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols)
 
 template <int D, bool kOutF32, bool kWin>
 cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, int64_t units, cudaStream_t st) {
+                       const CUtensorMap& mv, const CUtensorMap& mo, int64_t units, cudaStream_t st) {
   using L = Layout<D>;
   auto kern = attn_fwd_tc_kernel<D, kOutF32, kWin>;
   // setmaxnreg.inc waits until the registers it asks for are free in the block's
@@ -612,7 +659,7 @@ cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, co
   }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemRequest);
   if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_fwd_tc)");
-  kern<<<(unsigned)units, kThreads, L::kSmemRequest, st>>>(a, s, mq, mk, mv);
+  kern<<<(unsigned)units, kThreads, L::kSmemRequest, st>>>(a, s, mq, mk, mv, mo);
   return cuda_check(cudaGetLastError(), "attn_fwd_tc_kernel launch");
 }
 
@@ -631,20 +678,31 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
   if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * a.D)) != CP_OK) return r;
   if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;
   if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;
+  // O map (32-row boxes) over the output rows the schedule writes; without one
+  // (fp32 output, or a base the tensor map cannot take) rows are stored directly.
+  CUtensorMap mo;
+  memset(&mo, 0, sizeof(mo));
+  AttnArgs ao = a;
+  ao.o_tma = 0;
+  if (!a.o_f32) {
+    int64_t o_rows = 0;
+    for (int i = 0; i < s.n_groups; ++i) o_rows = std::max<int64_t>(o_rows, (int64_t)s.g[i].o_row0 + s.g[i].nq);
+    ao.o_tma = make_map(&mo, a.o, o_rows, a.o_ld, 32, false) == CP_OK ? 1 : 0;
+  }
   const bool win = a.window > 0;
   if (a.D == 128) {
     if (win)
-      return a.o_f32 ? launch_typed<128, true, true>(a, s, mq, mk, mv, units, st)
-                     : launch_typed<128, false, true>(a, s, mq, mk, mv, units, st);
-    return a.o_f32 ? launch_typed<128, true, false>(a, s, mq, mk, mv, units, st)
-                   : launch_typed<128, false, false>(a, s, mq, mk, mv, units, st);
+      return a.o_f32 ? launch_typed<128, true, true>(ao, s, mq, mk, mv, mo, units, st)
+                     : launch_typed<128, false, true>(ao, s, mq, mk, mv, mo, units, st);
+    return a.o_f32 ? launch_typed<128, true, false>(ao, s, mq, mk, mv, mo, units, st)
+                   : launch_typed<128, false, false>(ao, s, mq, mk, mv, mo, units, st);
   }
   if (a.D == 64) {
     if (win)
-      return a.o_f32 ? launch_typed<64, true, true>(a, s, mq, mk, mv, units, st)
-                     : launch_typed<64, false, true>(a, s, mq, mk, mv, units, st);
-    return a.o_f32 ? launch_typed<64, true, false>(a, s, mq, mk, mv, units, st)
-                   : launch_typed<64, false, false>(a, s, mq, mk, mv, units, st);
+      return a.o_f32 ? launch_typed<64, true, true>(ao, s, mq, mk, mv, mo, units, st)
+                     : launch_typed<64, false, true>(ao, s, mq, mk, mv, mo, units, st);
+    return a.o_f32 ? launch_typed<64, true, false>(ao, s, mq, mk, mv, mo, units, st)
+                   : launch_typed<64, false, false>(ao, s, mq, mk, mv, mo, units, st);
   }
   set_last_error("tcgen05 attention supports D = 64 or 128");
   return CP_ERR_UNSUPPORTED;

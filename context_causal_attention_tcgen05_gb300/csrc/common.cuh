@@ -76,6 +76,7 @@ struct AttnArgs {
   int32_t* err;       // device error word
   int32_t total_units;
   int32_t o_f32;      // output dtype: 1 fp32, 0 same as input
+  int32_t o_tma;      // bf16 output written by TMA stores through the launch's O tensor map
   int32_t window;     // sliding window (causal only): pos_q - pos_k < window; 0 = none
 };
 
@@ -228,6 +229,12 @@ __device__ __forceinline__ void doc_bounds(const int32_t* cu, int32_t n_docs, in
   *end = __ldg(cu + lo + 1);
 }
 
+// a / b for a >= 0, b > 0: one 32-bit division when both fit (positions and
+// strides of any buffer one GPU holds do), 64-bit otherwise.
+__device__ __forceinline__ int64_t udiv_pos(int64_t a, int64_t b) {
+  return ((uint64_t)a | (uint64_t)b) < 0x80000000ull ? (int64_t)((uint32_t)a / (uint32_t)b) : a / b;
+}
+
 // Tiles of `tile` rows over one schedule segment.  Positions grow with the row
 // index (pos_stride >= 1), so each visibility test below holds for a prefix or a
 // suffix of the segment's tiles and a range is found without walking them.
@@ -244,17 +251,17 @@ __device__ __forceinline__ void key_tile_range(const KSeg& sg, int tile, int64_t
   hi = (sg.nk + tile - 1) / tile;
   if (causal) {  // first key of the tile <= pq_hi
     const int64_t d = pq_hi - sg.pos_off;
-    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, udiv_pos(d, step) + 1);
   }
   if (docs) {  // first key of the tile < en_hi
     const int64_t d = en_hi - 1 - sg.pos_off;
-    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / step + 1);
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, udiv_pos(d, step) + 1);
   }
   lo = 0;
   const int64_t first = max(docs ? st_lo : INT64_MIN, win_lo);  // first position any query sees
   if (first != INT64_MIN && hi > 0) {  // last key of the tile >= first: a lower bound, then step forward
     const int64_t d = first - sg.pos_off;
-    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (d / sg.pos_stride - (tile - 1)) / tile));
+    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (udiv_pos(d, sg.pos_stride) - (tile - 1)) / tile));
     while (lo < hi) {
       const int n = min(tile, sg.nk - lo * tile);
       if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= first) break;
@@ -272,12 +279,12 @@ __device__ __forceinline__ void query_tile_range(const KSeg& sg, int tile, int64
   hi = (sg.nk + tile - 1) / tile;
   if (win_hi != INT64_MAX) {  // first query of the tile <= win_hi
     const int64_t d = win_hi - sg.pos_off;
-    hi = d < 0 ? 0 : (int)min((int64_t)hi, d / ((int64_t)sg.pos_stride * tile) + 1);
+    hi = d < 0 ? 0 : (int)min((int64_t)hi, udiv_pos(d, (int64_t)sg.pos_stride * tile) + 1);
   }
   lo = 0;
   if (causal) {  // last query of the tile >= pk_lo: a lower bound, then step forward
     const int64_t d = pk_lo - sg.pos_off;
-    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (d / sg.pos_stride - (tile - 1)) / tile));
+    if (d > 0) lo = (int)min((int64_t)hi, max((int64_t)0, (udiv_pos(d, sg.pos_stride) - (tile - 1)) / tile));
     while (lo < hi) {
       const int n = min(tile, sg.nk - lo * tile);
       if ((int64_t)sg.pos_off + (int64_t)sg.pos_stride * (lo * tile + n - 1) >= pk_lo) break;
