@@ -238,17 +238,14 @@ def bench_ours(args):
 
     def step(ev):
         ev[0].record(stream)
-        cpa.cp_zigzag_reorder(q, P, y=q_re)
-        cpa.cp_zigzag_reorder(k, P, y=k_re)
-        cpa.cp_zigzag_reorder(v, P, y=v_re)
+        cpa.cp_ring_reorder_qkv(q, k, v, P, layout, q_re=q_re, k_re=k_re, v_re=v_re)
         ev[1].record(stream)
         cpa.cp_ring_attention_reordered(q_re, k_re, v_re, P, layout, "fused", out=o_re, lse=lse_re)
         ev[2].record(stream)
-        cpa.cp_zigzag_restore(o_re, P, x=out)
-        cpa.cp_lse_reorder(lse_re, P, layout, inverse=True, y=lse)
+        cpa.cp_ring_restore(o_re, lse_re, P, layout, out=out, lse=lse)
         ev[3].record(stream)
 
-    launches_per_step = 6
+    launches_per_step = 3  # q/k/v reorder, attention, out + lse restore
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
     def timed(fn, reps):

@@ -23,7 +23,7 @@ __all__ = [
     "cp_attn_block_fwd", "cp_attn_block_bwd", "cp_attn_block_bwd_noalloc", "cp_lse_merge",
     "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
-    "cp_lse_reorder",
+    "cp_lse_reorder", "cp_ring_reorder_qkv", "cp_ring_restore",
     "cp_ring_attention", "cp_ring_attention_reordered", "cp_ring_attention_bwd", "cp_ulysses_attention",
     "cp_ulysses_attention_bwd", "cp_usp_attention",
     "cp_workspace_size", "cp_check_device_status", "cp_debug_bounded_wait",
@@ -63,6 +63,9 @@ _SIGS = {
     "cp_striped_reorder": [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
     "cp_striped_restore": [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
     "cp_lse_reorder": [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
+    "cp_ring_reorder_qkv": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32,
+                            _c_i32, _c_i32, _c_p],
+    "cp_ring_restore": [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p],
     "cp_ring_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                           _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ring_attention_reordered": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
@@ -299,6 +302,31 @@ def cp_lse_reorder(x, P, reorder="zigzag", inverse=False, y=None, stream=None):
     _check("cp_lse_reorder", load_library().cp_lse_reorder(
         _ptr(x), _ptr(y), S, H, P, REORDER[reorder], int(bool(inverse)), _stream(stream)))
     return y
+
+
+def cp_ring_reorder_qkv(q, k, v, P, reorder="zigzag", q_re=None, k_re=None, v_re=None, stream=None):
+    """q, k, v in sequence order -> the ranks' order, in one launch."""
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    q_re = torch.empty_like(q) if q_re is None else q_re
+    k_re = torch.empty_like(k) if k_re is None else k_re
+    v_re = torch.empty_like(v) if v_re is None else v_re
+    _check("cp_ring_reorder_qkv", load_library().cp_ring_reorder_qkv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(q_re), _ptr(k_re), _ptr(v_re), S, Hq, Hkv, D, _dt(q), P,
+        REORDER[reorder], _stream(stream)))
+    return q_re, k_re, v_re
+
+
+def cp_ring_restore(o_re, lse_re, P, reorder="zigzag", out=None, lse=None, stream=None):
+    """The ring's out (and lse, unless lse_re is None) back to sequence order, in one launch."""
+    S, Hq, D = o_re.shape
+    out = torch.empty_like(o_re) if out is None else out
+    if lse_re is not None and lse is None:
+        lse = torch.empty_like(lse_re)
+    _check("cp_ring_restore", load_library().cp_ring_restore(
+        _ptr(o_re), None if lse_re is None else _ptr(lse_re), _ptr(out), None if lse is None else _ptr(lse),
+        S, Hq, D, _dt(o_re), P, REORDER[reorder], _stream(stream)))
+    return out, lse
 
 
 def cp_ring_attention(q, k, v, P, reorder="auto", mode="fused", cu_seqlens=None, out=None, lse=None,

@@ -744,6 +744,77 @@ cp_status cp_striped_restore(const void* y, void* x, int64_t S, int32_t H, int32
   return permute_common(kStripedRestore, y, x, S, H, D, P, dtype, stream);
 }
 
+// The lse [H, S] column map of a zigzag reorder or restore as one gather job, when
+// every chunk is a whole number of 16-byte runs.
+static bool lse_cols_job(int row_kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,
+                         GatherJob& j) {
+  if (row_kind != kZigzagReorder && row_kind != kZigzagRestore) return false;
+  if ((S / (2 * P)) % 4 != 0) return false;
+  j = GatherJob{row_kind == kZigzagReorder ? kZigzagReorderCols : kZigzagRestoreCols, x, y, (int64_t)H,
+                S * 4, P};
+  return true;
+}
+
+static bool disjoint(const void* a, const void* b, size_t nbytes) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return x + nbytes <= y || y + nbytes <= x;
+}
+
+// Checks shared by the batched ring permutes; returns the row map kind.
+static cp_status ring_permute_check(int64_t S, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                                    int inverse, int* kind) {
+  CP_REQUIRE(reorder == CP_REORDER_DUAL_CHUNK_SWAP || reorder == CP_REORDER_STRIPED, CP_ERR_INVALID_ARG,
+             "reorder must be DUAL_CHUNK_SWAP or STRIPED");
+  CP_REQUIRE(dtype == CP_F32 || dtype == CP_BF16, CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  CP_REQUIRE(S >= 0 && D >= 1 && P >= 1 && P <= 1024, CP_ERR_INVALID_ARG, "bad sizes");
+  const bool zz = reorder == CP_REORDER_DUAL_CHUNK_SWAP;
+  CP_REQUIRE(S % (zz ? 2 * P : P) == 0, CP_ERR_SHAPE, "S must divide into the layout's chunks");
+  *kind = zz ? (inverse ? kZigzagRestore : kZigzagReorder) : (inverse ? kStripedRestore : kStripedReorder);
+  return CP_OK;
+}
+
+cp_status cp_ring_reorder_qkv(const void* q, const void* k, const void* v, void* q_re, void* k_re,
+                              void* v_re, int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                              int32_t P, int32_t reorder, void* stream) {
+  int kind = 0;
+  CP_TRY(ring_permute_check(S, D, dtype, P, reorder, 0, &kind));
+  CP_REQUIRE(Hq >= 1 && Hkv >= 1, CP_ERR_INVALID_ARG, "Hq >= 1 and Hkv >= 1 required");
+  const size_t qb = (size_t)Hq * D * dtype_size(dtype), kb = (size_t)Hkv * D * dtype_size(dtype);
+  CP_REQUIRE(qb % 16 == 0 && kb % 16 == 0, CP_ERR_ALIGN, "H*D*sizeof(dtype) must be a multiple of 16 bytes");
+  if (S == 0) return CP_OK;
+  CP_REQUIRE(q && k && v && q_re && k_re && v_re, CP_ERR_INVALID_ARG, "pointers must not be NULL");
+  CP_REQUIRE(disjoint(q, q_re, S * qb) && disjoint(k, k_re, S * kb) && disjoint(v, v_re, S * kb),
+             CP_ERR_INVALID_ARG, "each input and its reordered copy must not overlap");
+  GatherJob jobs[3] = {{kind, q, q_re, S, (int64_t)qb, P}, {kind, k, k_re, S, (int64_t)kb, P},
+                       {kind, v, v_re, S, (int64_t)kb, P}};
+  return launch_row_gather_batch(jobs, 3, (cudaStream_t)stream);
+}
+
+cp_status cp_ring_restore(const void* o_re, const float* lse_re, void* out, float* lse, int64_t S,
+                          int32_t Hq, int32_t D, int32_t dtype, int32_t P, int32_t reorder, void* stream) {
+  int kind = 0;
+  CP_TRY(ring_permute_check(S, D, dtype, P, reorder, 1, &kind));
+  CP_REQUIRE(Hq >= 1, CP_ERR_INVALID_ARG, "Hq >= 1 required");
+  CP_REQUIRE((uint64_t)S * Hq < (1ull << 32), CP_ERR_UNSUPPORTED, "S*Hq must be < 2^32");
+  const size_t ob = (size_t)Hq * D * dtype_size(dtype);
+  CP_REQUIRE(ob % 16 == 0, CP_ERR_ALIGN, "Hq*D*sizeof(dtype) must be a multiple of 16 bytes");
+  CP_REQUIRE((lse_re == nullptr) == (lse == nullptr), CP_ERR_INVALID_ARG,
+             "lse_re and lse must both be given or both be NULL");
+  if (S == 0) return CP_OK;
+  CP_REQUIRE(o_re && out, CP_ERR_INVALID_ARG, "o_re and out must not be NULL");
+  CP_REQUIRE(disjoint(o_re, out, S * ob), CP_ERR_INVALID_ARG, "o_re and out must not overlap");
+  if (lse)
+    CP_REQUIRE(disjoint(lse_re, lse, (size_t)S * Hq * 4), CP_ERR_INVALID_ARG, "lse_re and lse must not overlap");
+  cudaStream_t st = (cudaStream_t)stream;
+  GatherJob jobs[2] = {{kind, o_re, out, S, (int64_t)ob, P}, {}};
+  int n = 1;
+  if (lse && lse_cols_job(kind, lse_re, lse, S, Hq, P, jobs[1])) n = 2;
+  CP_TRY(launch_row_gather_batch(jobs, n, st));
+  if (lse && n == 1) CP_TRY(launch_lse_permute(kind, lse_re, lse, S, Hq, P, st));
+  return CP_OK;
+}
+
 cp_status cp_lse_reorder(const float* x, float* y, int64_t S, int32_t H, int32_t P,
                          int32_t reorder, int32_t inverse, void* stream) {
   CP_REQUIRE(reorder == CP_REORDER_DUAL_CHUNK_SWAP || reorder == CP_REORDER_STRIPED,
@@ -830,9 +901,10 @@ cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t
   // Contiguous layout: rank r already holds rows [rC, (r+1)C) in place.
   const bool moved = layout != CP_REORDER_CONTIGUOUS;
   if (moved) {
-    CP_TRY(launch_row_gather(fwd_kind, q, q_re, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_row_gather(fwd_kind, k, k_re, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(fwd_kind, v, v_re, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    GatherJob jobs[3] = {{fwd_kind, q, q_re, S, (int64_t)Hq * D * (int64_t)es, P},
+                         {fwd_kind, k, k_re, S, (int64_t)Hkv * D * (int64_t)es, P},
+                         {fwd_kind, v, v_re, S, (int64_t)Hkv * D * (int64_t)es, P}};
+    CP_TRY(launch_row_gather_batch(jobs, 3, st));
   } else {
     q_re = const_cast<void*>(q);
     k_re = const_cast<void*>(k);
@@ -843,8 +915,10 @@ cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t
   CP_TRY(ring_core(q_re, k_re, v_re, o_re, lse_re, S, Hq, Hkv, D, dtype, P, layout, mode,
                    cu_seqlens, n_docs, ws_at(workspace, w.partials), w.pw, st));
   if (moved) {
-    CP_TRY(launch_row_gather(back_kind, o_re, out, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_lse_permute(back_kind, lse_re, lse, S, Hq, P, st));
+    GatherJob jobs[2] = {{back_kind, o_re, out, S, (int64_t)Hq * D * (int64_t)es, P}, {}};
+    const int n = lse_cols_job(back_kind, lse_re, lse, S, Hq, P, jobs[1]) ? 2 : 1;
+    CP_TRY(launch_row_gather_batch(jobs, n, st));
+    if (n == 1) CP_TRY(launch_lse_permute(back_kind, lse_re, lse, S, Hq, P, st));
   }
   return CP_OK;
 }
@@ -913,12 +987,13 @@ cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, con
     void* ow = ws_at(workspace, w.o);
     void* dw = ws_at(workspace, w.dout);
     float* lw = reinterpret_cast<float*>(ws_at(workspace, w.lse));
-    CP_TRY(launch_row_gather(fwd_kind, q, qw, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_row_gather(fwd_kind, k, kw, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(fwd_kind, v, vw, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(fwd_kind, out, ow, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_row_gather(fwd_kind, dout, dw, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_lse_permute(fwd_kind, lse, lw, S, Hq, P, st));
+    const int64_t qb = (int64_t)Hq * D * (int64_t)es, kb = (int64_t)Hkv * D * (int64_t)es;
+    GatherJob jobs[6] = {{fwd_kind, q, qw, S, qb, P},   {fwd_kind, k, kw, S, kb, P},
+                         {fwd_kind, v, vw, S, kb, P},   {fwd_kind, out, ow, S, qb, P},
+                         {fwd_kind, dout, dw, S, qb, P}, {}};
+    const int n = lse_cols_job(fwd_kind, lse, lw, S, Hq, P, jobs[5]) ? 6 : 5;
+    CP_TRY(launch_row_gather_batch(jobs, n, st));
+    if (n == 5) CP_TRY(launch_lse_permute(fwd_kind, lse, lw, S, Hq, P, st));
     q_re = qw; k_re = kw; v_re = vw; o_re = ow; do_re = dw; lse_re = lw;
   }
   float* delta = reinterpret_cast<float*>(ws_at(workspace, w.delta));
@@ -950,9 +1025,10 @@ cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, con
     CP_TRY(launch_cast_out(dq_acc, dq_c, S * Hq * D, is_bf16, st));
     CP_TRY(launch_cast_out(dk_acc, dk_c, S * Hkv * D, is_bf16, st));
     CP_TRY(launch_cast_out(dv_acc, dv_c, S * Hkv * D, is_bf16, st));
-    CP_TRY(launch_row_gather(back_kind, dq_c, dq, S, (int64_t)Hq * D * es, P, Hq, st));
-    CP_TRY(launch_row_gather(back_kind, dk_c, dk, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(back_kind, dv_c, dv, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    GatherJob jobs[3] = {{back_kind, dq_c, dq, S, (int64_t)Hq * D * (int64_t)es, P},
+                         {back_kind, dk_c, dk, S, (int64_t)Hkv * D * (int64_t)es, P},
+                         {back_kind, dv_c, dv, S, (int64_t)Hkv * D * (int64_t)es, P}};
+    CP_TRY(launch_row_gather_batch(jobs, 3, st));
   } else {
     CP_TRY(launch_cast_out(dq_acc, dq, S * Hq * D, is_bf16, st));
     CP_TRY(launch_cast_out(dk_acc, dk, S * Hkv * D, is_bf16, st));
@@ -994,11 +1070,13 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   void* kh = ws_at(workspace, w.k);
   void* vh = ws_at(workspace, w.v);
   void* oh = ws_at(workspace, w.o);
-  CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
   if (R == 1) {
-    CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
+    GatherJob jobs[3] = {{kSeq2Head, q, qh, S, (int64_t)Hq * D * (int64_t)es, P},
+                         {kSeq2Head, k, kh, S, (int64_t)Hkv * D * (int64_t)es, P},
+                         {kSeq2Head, v, vh, S, (int64_t)Hkv * D * (int64_t)es, P}};
+    CP_TRY(launch_row_gather_batch(jobs, 3, st));
   } else {  // rank p gets a copy of key/value head p / R
+    CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
     CP_TRY(launch_kv_replicate(k, kh, S, Hkv, (int64_t)D * es, P, st));
     CP_TRY(launch_kv_replicate(v, vh, S, Hkv, (int64_t)D * es, P, st));
   }
@@ -1055,9 +1133,10 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
   const int back_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagRestore : kStripedRestore;
   const void *q_re = q, *k_re = k, *v_re = v;
   if (moved) {  // the ring's partition across groups
-    CP_TRY(launch_row_gather(fwd_kind, q, ws_at(workspace, w.q_re), S, (int64_t)Hq * D * es, P_ring, Hq, st));
-    CP_TRY(launch_row_gather(fwd_kind, k, ws_at(workspace, w.k_re), S, (int64_t)Hkv * D * es, P_ring, Hkv, st));
-    CP_TRY(launch_row_gather(fwd_kind, v, ws_at(workspace, w.v_re), S, (int64_t)Hkv * D * es, P_ring, Hkv, st));
+    GatherJob jobs[3] = {{fwd_kind, q, ws_at(workspace, w.q_re), S, (int64_t)Hq * D * (int64_t)es, P_ring},
+                         {fwd_kind, k, ws_at(workspace, w.k_re), S, (int64_t)Hkv * D * (int64_t)es, P_ring},
+                         {fwd_kind, v, ws_at(workspace, w.v_re), S, (int64_t)Hkv * D * (int64_t)es, P_ring}};
+    CP_TRY(launch_row_gather_batch(jobs, 3, st));
     q_re = ws_at(workspace, w.q_re);
     k_re = ws_at(workspace, w.k_re);
     v_re = ws_at(workspace, w.v_re);
@@ -1066,9 +1145,12 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
   void* qh = ws_at(workspace, w.qh);
   void* kh = ws_at(workspace, w.kh);
   void* vh = ws_at(workspace, w.vh);
-  CP_TRY(launch_row_gather(kSeq2Head, q_re, qh, S, (int64_t)Hq * D * es, P_ulysses, Hq, st));
-  CP_TRY(launch_row_gather(kSeq2Head, k_re, kh, S, (int64_t)Hkv * D * es, P_ulysses, Hkv, st));
-  CP_TRY(launch_row_gather(kSeq2Head, v_re, vh, S, (int64_t)Hkv * D * es, P_ulysses, Hkv, st));
+  {
+    GatherJob jobs[3] = {{kSeq2Head, q_re, qh, S, (int64_t)Hq * D * (int64_t)es, P_ulysses},
+                         {kSeq2Head, k_re, kh, S, (int64_t)Hkv * D * (int64_t)es, P_ulysses},
+                         {kSeq2Head, v_re, vh, S, (int64_t)Hkv * D * (int64_t)es, P_ulysses}};
+    CP_TRY(launch_row_gather_batch(jobs, 3, st));
+  }
   // the fused ring across groups, once per head share, in one launch
   Schedule* ring = new Schedule;
   Schedule* s = new Schedule;
@@ -1167,12 +1249,14 @@ cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const void* v, 
   // head_to_seq is the backward of seq_to_head: the gradients take the same
   // exchange as the outputs.  Delta = rowsum(dO o O) on the sequence layout
   // (same [Hq, S] order as lse), then both go to the head-major row order.
-  CP_TRY(launch_row_gather(kSeq2Head, q, qh, S, (int64_t)Hq * D * es, P, Hq, st));
-  CP_TRY(launch_row_gather(kSeq2Head, dout, doh, S, (int64_t)Hq * D * es, P, Hq, st));
-  if (R == 1) {
-    CP_TRY(launch_row_gather(kSeq2Head, k, kh, S, (int64_t)Hkv * D * es, P, Hkv, st));
-    CP_TRY(launch_row_gather(kSeq2Head, v, vh, S, (int64_t)Hkv * D * es, P, Hkv, st));
-  } else {
+  {
+    GatherJob jobs[4] = {{kSeq2Head, q, qh, S, (int64_t)Hq * D * (int64_t)es, P},
+                         {kSeq2Head, dout, doh, S, (int64_t)Hq * D * (int64_t)es, P},
+                         {kSeq2Head, k, kh, S, (int64_t)Hkv * D * (int64_t)es, P},
+                         {kSeq2Head, v, vh, S, (int64_t)Hkv * D * (int64_t)es, P}};
+    CP_TRY(launch_row_gather_batch(jobs, R == 1 ? 4 : 2, st));
+  }
+  if (R > 1) {
     CP_TRY(launch_kv_replicate(k, kh, S, Hkv, (int64_t)D * es, P, st));
     CP_TRY(launch_kv_replicate(v, vh, S, Hkv, (int64_t)D * es, P, st));
   }

@@ -118,6 +118,21 @@ cp_status cuda_check(cudaError_t e, const char* what);
 // movers.cu
 cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t row_bytes,
                             int32_t P, int32_t H_for_ulysses, cudaStream_t st);
+
+// One gather of a batch: S rows of row_bytes from x to y with the row map of `kind`
+// (a GatherKind) over P ranks.  For the *Cols kinds S counts lse heads and
+// row_bytes is one lse row (sequence length x 4).
+struct GatherJob {
+  int kind;
+  const void* x;
+  void* y;
+  int64_t S;
+  int64_t row_bytes;
+  int32_t P;
+};
+constexpr int kMaxGatherBatch = 6;
+// Runs 1..kMaxGatherBatch gathers in one launch.
+cp_status launch_row_gather_batch(const GatherJob* jobs, int n, cudaStream_t st);
 cp_status launch_lse_permute(int kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,
                              cudaStream_t st);
 // merge.cu
@@ -155,6 +170,8 @@ enum GatherKind : int {
   kSeq2Head = 4,
   kHead2Seq = 5,
   kSeq2HeadRep = 6,  // Ulysses seq2head of key/value heads replicated P/Hkv times
+  kZigzagReorderCols = 7,  // the zigzag maps on the columns of an lse [H, S] fp32 array,
+  kZigzagRestoreCols = 8,  // as 16-byte runs (needs S/(2P) % 4 == 0)
 };
 
 // Fills group tile prefix sums for a query tile height; returns total units (tiles x heads).

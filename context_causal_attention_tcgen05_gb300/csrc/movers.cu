@@ -15,7 +15,10 @@
 // stores are fully coalesced and loads are coalesced within a run (runs are
 // >= 512 bytes at the model shapes).  Loads and stores bypass L1 and are
 // marked streaming: every byte is touched exactly once.
+#include <string.h>
+
 #include <algorithm>
+#include <string>
 
 #include "common.cuh"
 
@@ -33,15 +36,32 @@ struct GatherParams {
   int kind;
 };
 
+// Several gathers in one launch: blocks [block0[i], block0[i+1]) serve gather i.
+struct GatherBatch {
+  GatherParams t[kMaxGatherBatch];
+  uint32_t block0[kMaxGatherBatch + 1];
+  int32_t n;
+};
+
+__device__ __forceinline__ uint32_t zigzag_slot_source(uint32_t u, uint32_t P) {
+  uint32_t r = u >> 1, j = u & 1;  // slot u = (rank r, half j) <- chunk j ? 2P-1-r : r
+  return j ? (2 * P - 1 - r) : r;
+}
+__device__ __forceinline__ uint32_t zigzag_chunk_source(uint32_t c, uint32_t P) {
+  return c < P ? 2 * c : 2 * (2 * P - 1 - c) + 1;  // chunk c <- its (rank, half) slot
+}
+
 __device__ __forceinline__ uint32_t source_run(const GatherParams& p, uint32_t u) {
   switch (p.kind) {
-    case kZigzagReorder: {  // out run u = (rank r = u/2, half j = u%2) <- chunk j ? 2P-1-r : r
-      uint32_t r = u >> 1, j = u & 1;
-      return j ? (2 * p.P - 1 - r) : r;
-    }
-    case kZigzagRestore: {  // out run = chunk c <- (rank, half) slot
-      uint32_t c = u;
-      return c < p.P ? 2 * c : 2 * (2 * p.P - 1 - c) + 1;
+    case kZigzagReorder:  // out run u = (rank r = u/2, half j = u%2) <- chunk j ? 2P-1-r : r
+      return zigzag_slot_source(u, p.P);
+    case kZigzagRestore:  // out run = chunk c <- (rank, half) slot
+      return zigzag_chunk_source(u, p.P);
+    case kZigzagReorderCols:  // lse [H, S]: run u = (head h, slot) of 2P per head row
+    case kZigzagRestoreCols: {
+      uint32_t h = u / (2 * p.P), c = u - h * 2 * p.P;
+      return h * 2 * p.P +
+             (p.kind == kZigzagReorderCols ? zigzag_slot_source(c, p.P) : zigzag_chunk_source(c, p.P));
     }
     case kStripedReorder: {  // out row u = r*(S/P) + i <- in row i*P + r
       uint32_t r = u / p.a, i = u - r * p.a;
@@ -69,8 +89,11 @@ __device__ __forceinline__ uint32_t source_run(const GatherParams& p, uint32_t u
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 4;
 
-__global__ void __launch_bounds__(kThreads) row_gather_kernel(GatherParams p) {
-  uint32_t base = blockIdx.x * (kThreads * kVecPerThread) + threadIdx.x;
+__global__ void __launch_bounds__(kThreads) row_gather_kernel(const __grid_constant__ GatherBatch bt) {
+  int ti = 0;
+  while (ti + 1 < bt.n && blockIdx.x >= bt.block0[ti + 1]) ++ti;
+  const GatherParams& p = bt.t[ti];
+  uint32_t base = (blockIdx.x - bt.block0[ti]) * (kThreads * kVecPerThread) + threadIdx.x;
   int4 buf[kVecPerThread];
   uint32_t dst[kVecPerThread];
 #pragma unroll
@@ -182,7 +205,87 @@ __global__ void __launch_bounds__(256) heads_to_seq_sum_kernel(const float* src,
   }
 }
 
+// One launch for n gathers (n <= kMaxGatherBatch), blocks split by output size.
+cp_status launch_gathers(const GatherParams* ps, int n, cudaStream_t st, const char* what) {
+  GatherBatch bt;
+  memset(&bt, 0, sizeof(bt));
+  const uint32_t per_block = kThreads * kVecPerThread;
+  uint64_t blocks = 0;
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (ps[i].total_vec == 0) continue;
+    bt.t[m] = ps[i];
+    bt.block0[m] = (uint32_t)blocks;
+    blocks += (ps[i].total_vec + per_block - 1) / per_block;
+    ++m;
+  }
+  if (m == 0) return CP_OK;
+  if (blocks >= (1ull << 31)) {
+    set_last_error("permute launch too large");
+    return CP_ERR_UNSUPPORTED;
+  }
+  bt.block0[m] = (uint32_t)blocks;
+  bt.n = m;
+  row_gather_kernel<<<(uint32_t)blocks, kThreads, 0, st>>>(bt);
+  return cuda_check(cudaGetLastError(), what);
+}
+
+// Gather parameters of one job (row maps as in source_run).
+cp_status fill_gather(const GatherJob& j, GatherParams& p) {
+  p.x = static_cast<const int4*>(j.x);
+  p.y = static_cast<int4*>(j.y);
+  p.P = (uint32_t)j.P;
+  p.b = 0;
+  p.kind = j.kind;
+  uint64_t total_bytes = (uint64_t)j.S * (uint64_t)j.row_bytes;
+  uint64_t total_vec = total_bytes / 16;
+  if (total_vec >= (1ull << 32)) {
+    set_last_error("tensor larger than 64 GiB is not supported by the permute kernels");
+    return CP_ERR_UNSUPPORTED;
+  }
+  p.total_vec = (uint32_t)total_vec;
+  switch (j.kind) {
+    case kZigzagReorder:
+    case kZigzagRestore:
+      p.run_vec = (uint32_t)(total_vec / (2 * (uint64_t)j.P));
+      p.a = (uint32_t)j.P;
+      break;
+    case kZigzagReorderCols:  // S = heads, row_bytes = one lse row; 2P runs per row
+    case kZigzagRestoreCols:
+      p.run_vec = (uint32_t)(j.row_bytes / (2 * j.P) / 16);
+      p.a = (uint32_t)j.P;
+      break;
+    case kStripedReorder:
+    case kStripedRestore:
+      p.run_vec = (uint32_t)(j.row_bytes / 16);
+      p.a = (uint32_t)(j.S / j.P);
+      break;
+    default:  // Ulysses: runs of H/P heads
+      p.run_vec = (uint32_t)(j.row_bytes / j.P / 16);  // (H/P)*D elements
+      p.a = (uint32_t)j.S;
+      break;
+  }
+  return CP_OK;
+}
+
 }  // namespace
+
+cp_status launch_row_gather_batch(const GatherJob* jobs, int n, cudaStream_t st) {
+  if (n < 1 || n > kMaxGatherBatch) {
+    set_last_error("a permute batch holds 1 to " + std::to_string(kMaxGatherBatch) + " tensors");
+    return CP_ERR_INVALID_ARG;
+  }
+  GatherParams ps[kMaxGatherBatch];
+  for (int i = 0; i < n; ++i) {
+    if (jobs[i].S == 0) {
+      ps[i].total_vec = 0;
+      continue;
+    }
+    cp_status r = fill_gather(jobs[i], ps[i]);
+    if (r != CP_OK) return r;
+  }
+  return launch_gathers(ps, n, st, "row_gather_kernel launch");
+}
 
 cp_status launch_kv_replicate(const void* x, void* y, int64_t S, int32_t Hkv, int64_t head_bytes,
                               int32_t P, cudaStream_t st) {
@@ -201,10 +304,7 @@ cp_status launch_kv_replicate(const void* x, void* y, int64_t S, int32_t Hkv, in
     return CP_ERR_UNSUPPORTED;
   }
   p.total_vec = (uint32_t)total_vec;
-  uint32_t per_block = kThreads * kVecPerThread;
-  uint32_t blocks = (p.total_vec + per_block - 1) / per_block;
-  row_gather_kernel<<<blocks, kThreads, 0, st>>>(p);
-  return cuda_check(cudaGetLastError(), "row_gather_kernel launch (replicated seq2head)");
+  return launch_gathers(&p, 1, st, "row_gather_kernel launch (replicated seq2head)");
 }
 
 cp_status launch_lse_to_heads(const float* x, float* y, int64_t S, int32_t H, int32_t P,
@@ -233,40 +333,9 @@ cp_status launch_heads_to_seq_sum(const float* src, void* dst, int64_t S, int32_
 
 cp_status launch_row_gather(int kind, const void* x, void* y, int64_t S, int64_t row_bytes,
                             int32_t P, int32_t H_for_ulysses, cudaStream_t st) {
-  if (S == 0) return CP_OK;
-  GatherParams p;
-  p.x = static_cast<const int4*>(x);
-  p.y = static_cast<int4*>(y);
-  p.P = (uint32_t)P;
-  p.b = 0;
-  p.kind = kind;
-  uint64_t total_bytes = (uint64_t)S * (uint64_t)row_bytes;
-  uint64_t total_vec = total_bytes / 16;
-  if (total_vec >= (1ull << 32)) {
-    set_last_error("tensor larger than 64 GiB is not supported by the permute kernels");
-    return CP_ERR_UNSUPPORTED;
-  }
-  p.total_vec = (uint32_t)total_vec;
-  switch (kind) {
-    case kZigzagReorder:
-    case kZigzagRestore:
-      p.run_vec = (uint32_t)(total_vec / (2 * (uint64_t)P));
-      p.a = (uint32_t)P;
-      break;
-    case kStripedReorder:
-    case kStripedRestore:
-      p.run_vec = (uint32_t)(row_bytes / 16);
-      p.a = (uint32_t)(S / P);
-      break;
-    default:  // Ulysses: runs of H/P heads
-      p.run_vec = (uint32_t)(row_bytes / P / 16);  // (H/P)*D elements
-      p.a = (uint32_t)S;
-      break;
-  }
-  uint32_t per_block = kThreads * kVecPerThread;
-  uint32_t blocks = (p.total_vec + per_block - 1) / per_block;
-  row_gather_kernel<<<blocks, kThreads, 0, st>>>(p);
-  return cuda_check(cudaGetLastError(), "row_gather_kernel launch");
+  (void)H_for_ulysses;
+  GatherJob j{kind, x, y, S, row_bytes, P};
+  return launch_row_gather_batch(&j, 1, st);
 }
 
 cp_status launch_lse_permute(int kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,

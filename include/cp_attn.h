@@ -207,6 +207,24 @@ CP_API cp_status cp_striped_restore(const void* y, void* x, int64_t S, int32_t H
 CP_API cp_status cp_lse_reorder(const float* x, float* y, int64_t S, int32_t H, int32_t P,
                                 int32_t reorder, int32_t inverse, void* stream);
 
+/* The ring's input and output permutes of one pass in one launch each (the
+ * handbook's "The zigzag partition" and the MaxText packing PR's STRIPED
+ * strategy; reorder is CP_REORDER_DUAL_CHUNK_SWAP or CP_REORDER_STRIPED).
+ * cp_ring_reorder_qkv: q [S,Hq,D] -> q_re, k/v [S,Hkv,D] -> k_re/v_re in the
+ * ranks' order, the row map of cp_zigzag_reorder / cp_striped_reorder.
+ * cp_ring_restore: o_re [S,Hq,D] -> out and lse_re [Hq,S] -> lse back in
+ * sequence order (lse_re and lse may both be NULL: out only).  Device
+ * pointers, caller-owned; a source and its destination must not overlap.
+ * Bit-exact copies; results equal the single-tensor calls.  Errors:
+ * CP_ERR_INVALID_ARG (layout, NULL, overlap), CP_ERR_SHAPE (S not a multiple
+ * of 2P / P), CP_ERR_ALIGN (H*D*sizeof(dtype) not a multiple of 16 bytes). */
+CP_API cp_status cp_ring_reorder_qkv(const void* q, const void* k, const void* v, void* q_re, void* k_re,
+                                     void* v_re, int64_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                                     int32_t dtype, int32_t P, int32_t reorder, void* stream);
+CP_API cp_status cp_ring_restore(const void* o_re, const float* lse_re, void* out, float* lse, int64_t S,
+                                 int32_t Hq, int32_t D, int32_t dtype, int32_t P, int32_t reorder,
+                                 void* stream);
+
 /* ---------------------------------------------------------------- drivers */
 
 /* Causal ring attention over P virtual ranks ("Ring Attention" with the

@@ -156,6 +156,26 @@ def test_permute_refusals(lib):
     assert lib.cp_zigzag_reorder(P16, P16, 0, 8, 128, 4, 1, None) == 0       # empty
 
 
+def test_batched_ring_permute_refusals(lib):
+    P32 = ctypes.c_void_p((1 << 20) + (1 << 30))  # a second fake address, far from P16
+    qkv = lambda S=64, Hq=8, Hkv=8, D=128, dt=1, P=4, reo=1, dst=P32: lib.cp_ring_reorder_qkv(
+        P16, P16, P16, dst, dst, dst, S, Hq, Hkv, D, dt, P, reo, None)
+    assert qkv(reo=0) == -1          # contiguous: nothing to reorder
+    assert qkv(reo=3) == -1          # AUTO needs documents to resolve
+    assert qkv(S=60) == -2           # S % 2P
+    assert qkv(S=60, reo=2, dst=P16) == -1  # striped needs only S % P; then the overlap check
+    assert qkv(D=4, Hkv=1) == -4     # 8-byte rows of k/v
+    assert qkv(dt=7) == -3
+    assert qkv(dst=P16) == -1        # source and destination overlap
+    assert qkv(S=0) == 0             # empty
+    rst = lambda S=64, lse_re=P16, lse=P32, P=4, reo=1: lib.cp_ring_restore(
+        P16, lse_re, P32, lse, S, 8, 128, 1, P, reo, None)
+    assert rst(lse=None) == -1       # lse_re without lse
+    assert rst(reo=0) == -1
+    assert rst(S=60) == -2
+    assert rst(S=0) == 0
+
+
 def test_merge_and_workspace_refusals(lib):
     assert lib.cp_lse_merge(P16, P16, P16, P16, P16, P16, 16, 4, 100, 1, None) == -4
     assert lib.cp_lse_merge(P16, P16, P16, P16, P16, P16, 16, 4, 128, 5, None) == -3

@@ -243,3 +243,28 @@ def test_lse_reorder_bitexact(S, H, P):
         back = cpa.cp_lse_reorder(y, P, layout, inverse=True)
         assert torch.equal(back.cpu(), x)
     check_ok()
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,D,P,dtype", [
+    (64, 4, 2, 64, 4, torch.bfloat16),      # chunk of 8 rows: lse chunks of 8 floats (16-byte runs)
+    (72, 4, 4, 32, 6, torch.float32),       # chunk of 6 rows: lse by the column kernel
+    (8192, 32, 8, 128, 8, torch.bfloat16),  # the ring workload's shape, GQA
+])
+def test_batched_ring_permutes_bitexact(S, Hq, Hkv, D, P, dtype):
+    # one launch for q, k, v (and one for out + lse) equals the single-tensor calls and the oracle's maps
+    g = torch.Generator().manual_seed(17)
+    q = torch.randn(S, Hq, D, generator=g).to(dtype)
+    k = torch.randn(S, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(S, Hkv, D, generator=g).to(dtype)
+    lse = torch.randn(Hq, S, generator=g)
+    for layout in ("zigzag", "striped"):
+        qr, kr, vr = cpa.cp_ring_reorder_qkv(q.cuda(), k.cuda(), v.cuda(), P, layout)
+        for got, x in ((qr, q), (kr, k), (vr, v)):
+            want = oracle.reorder(x.float().numpy(), P, layout)
+            assert np.array_equal(got.float().cpu().numpy(), want), layout
+        lre = cpa.cp_lse_reorder(lse.cuda(), P, layout)
+        out, lse_back = cpa.cp_ring_restore(qr, lre, P, layout)
+        assert torch.equal(out.cpu(), q) and torch.equal(lse_back.cpu(), lse), layout
+        out2, none = cpa.cp_ring_restore(kr, None, P, layout)
+        assert none is None and torch.equal(out2.cpu(), k)
+    check_ok()
