@@ -745,11 +745,12 @@ cp_status cp_striped_restore(const void* y, void* x, int64_t S, int32_t H, int32
 }
 
 // The lse [H, S] column map of a zigzag reorder or restore as one gather job, when
-// every chunk is a whole number of 16-byte runs.
+// every chunk is a whole number of 16-byte runs and both arrays are 16-byte aligned
+// (otherwise the column kernel, which moves single floats, does it).
 static bool lse_cols_job(int row_kind, const float* x, float* y, int64_t S, int32_t H, int32_t P,
                          GatherJob& j) {
   if (row_kind != kZigzagReorder && row_kind != kZigzagRestore) return false;
-  if ((S / (2 * P)) % 4 != 0) return false;
+  if ((S / (2 * P)) % 4 != 0 || !aligned16(x) || !aligned16(y)) return false;
   j = GatherJob{row_kind == kZigzagReorder ? kZigzagReorderCols : kZigzagRestoreCols, x, y, (int64_t)H,
                 S * 4, P};
   return true;
@@ -783,7 +784,12 @@ cp_status cp_ring_reorder_qkv(const void* q, const void* k, const void* v, void*
   const size_t qb = (size_t)Hq * D * dtype_size(dtype), kb = (size_t)Hkv * D * dtype_size(dtype);
   CP_REQUIRE(qb % 16 == 0 && kb % 16 == 0, CP_ERR_ALIGN, "H*D*sizeof(dtype) must be a multiple of 16 bytes");
   if (S == 0) return CP_OK;
-  CP_REQUIRE(q && k && v && q_re && k_re && v_re, CP_ERR_INVALID_ARG, "pointers must not be NULL");
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(q_re, "q_re", false);
+  CP_CHECK_T(k_re, "k_re", false);
+  CP_CHECK_T(v_re, "v_re", false);
   CP_REQUIRE(disjoint(q, q_re, S * qb) && disjoint(k, k_re, S * kb) && disjoint(v, v_re, S * kb),
              CP_ERR_INVALID_ARG, "each input and its reordered copy must not overlap");
   GatherJob jobs[3] = {{kind, q, q_re, S, (int64_t)qb, P}, {kind, k, k_re, S, (int64_t)kb, P},
@@ -802,7 +808,8 @@ cp_status cp_ring_restore(const void* o_re, const float* lse_re, void* out, floa
   CP_REQUIRE((lse_re == nullptr) == (lse == nullptr), CP_ERR_INVALID_ARG,
              "lse_re and lse must both be given or both be NULL");
   if (S == 0) return CP_OK;
-  CP_REQUIRE(o_re && out, CP_ERR_INVALID_ARG, "o_re and out must not be NULL");
+  CP_CHECK_T(o_re, "o_re", false);
+  CP_CHECK_T(out, "out", false);
   CP_REQUIRE(disjoint(o_re, out, S * ob), CP_ERR_INVALID_ARG, "o_re and out must not overlap");
   if (lse)
     CP_REQUIRE(disjoint(lse_re, lse, (size_t)S * Hq * 4), CP_ERR_INVALID_ARG, "lse_re and lse must not overlap");

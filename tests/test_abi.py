@@ -168,12 +168,15 @@ def test_batched_ring_permute_refusals(lib):
     assert qkv(dt=7) == -3
     assert qkv(dst=P16) == -1        # source and destination overlap
     assert qkv(S=0) == 0             # empty
+    odd = ctypes.c_void_p((1 << 20) + (1 << 30) + 8)  # 8-byte aligned only
+    assert qkv(dst=odd) == -4        # 16-byte vectors need 16-byte aligned tensors
     rst = lambda S=64, lse_re=P16, lse=P32, P=4, reo=1: lib.cp_ring_restore(
         P16, lse_re, P32, lse, S, 8, 128, 1, P, reo, None)
     assert rst(lse=None) == -1       # lse_re without lse
     assert rst(reo=0) == -1
     assert rst(S=60) == -2
     assert rst(S=0) == 0
+    assert lib.cp_ring_restore(P16, P16, odd, P32, 64, 8, 128, 1, 4, 1, None) == -4  # out misaligned
 
 
 def test_merge_and_workspace_refusals(lib):

@@ -194,6 +194,22 @@ def test_ring_bwd_bf16_medium(layout, docs):
     check_ok()
 
 
+def test_ring_bwd_lse_not_16_byte_aligned():
+    # lse is only 4-byte aligned: its reorder takes the single-float column kernel
+    S, Hq, Hkv, D, P = 512, 2, 1, 128, 4
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=8, with_dout=True)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag")
+    buf = torch.empty(Hq * S + 4, dtype=torch.float32, device="cuda")
+    l_odd = buf[1:1 + Hq * S].view(Hq, S)
+    l_odd.copy_(l)
+    assert l_odd.data_ptr() % 16 != 0
+    dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l_odd, do.cuda(), P, "zigzag")
+    rq, rk, rv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, "zigzag")
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert torch.equal(got, ref)
+    check_ok()
+
+
 # ---------------------------------------------------------------- full-size workloads, sampled rows
 
 def _sampled_check(q, k, v, o, l, rows, cu=None, what=""):
