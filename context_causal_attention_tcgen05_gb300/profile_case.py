@@ -21,7 +21,7 @@ import context_causal_attention_tcgen05_gb300 as cpa
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["ring_fwd", "ring_bwd", "permute", "ulysses", "merge"], required=True)
+    ap.add_argument("--case", choices=["ring_fwd", "ring_bwd", "permute", "reorder_qkv", "ulysses", "merge"], required=True)
     ap.add_argument("--S", type=int, default=8192)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=32)
@@ -57,6 +57,10 @@ def main(argv=None) -> int:
         l2 = torch.randn(a.Hq, a.S, device="cuda", generator=g)
         for _ in range(a.reps):
             cpa.cp_lse_merge(o1, l1, o2, l2, out=o1, lse=l1)
+    elif a.case == "reorder_qkv":  # the ring step's input permute: q, k, v in one launch
+        ys = [torch.empty_like(x) for x in (q, k, v)]
+        for _ in range(a.reps):
+            cpa.cp_ring_reorder_qkv(q, k, v, a.P, a.layout, q_re=ys[0], k_re=ys[1], v_re=ys[2])
     elif a.case == "permute":
         y = torch.empty_like(q)
         for _ in range(a.reps):
