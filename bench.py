@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -167,6 +168,21 @@ def _oracle_rows(qs, ks, vs, n, rng):
     return 4.0 * D * H * float(np.sum(rows + 1)), dt
 
 
+def host_info() -> dict:
+    """The oracle timing host: CPUs in this process's affinity mask, all CPUs, and
+    the BLAS numpy was built against (its thread pool runs the oracle's products)."""
+    info = {"affinity_cpus": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None,
+            "cpu_count": os.cpu_count(), "machine": platform.machine()}
+    try:
+        import numpy as np
+        cfg = np.show_config(mode="dicts")
+        blas = cfg.get("Build Dependencies", {}).get("blas", {})
+        info["blas"] = f"{blas.get('name', '?')} {blas.get('version', '')}".strip()
+    except Exception:  # older numpy: no dict form
+        info["blas"] = "unknown"
+    return info
+
+
 def cpu_oracle_sample(q, k, v, target_s: float = 12.0):
     """Oracle throughput on a bounded sample sized to about target_s seconds.
     Returns (TFLOP/s, rows, seconds)."""
@@ -205,7 +221,8 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seed 0",
         "config": {"workload": WORKLOAD, "S": S, "H": H, "D": D, "P": P, "reorder": "dual_chunk_swap"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} random query rows x {H} heads per step, full causal key range"},
+                         "sample": f"{n} random query rows x {H} heads per step, full causal key range",
+                         "host": host_info()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -582,7 +599,8 @@ def bench_ours(args):
         if cpu_tf is not None:
             line["cpu_baseline"] = {"value": cpu_tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                     "sample": f"{cpu_rows} random query rows x {H} heads, full causal key "
-                                              f"range ({cpu_s:.1f} s of float64 CPU work)"}
+                                              f"range ({cpu_s:.1f} s of float64 CPU work)",
+                                    "host": host_info()}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

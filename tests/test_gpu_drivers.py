@@ -225,7 +225,7 @@ def test_full_ring_fwd_mha_s8192_p8_zigzag():
     q, k, v = make_inputs(S, H, H, D, torch.bfloat16, seed=0)
     o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag", "fused")
     check_ok()
-    _sampled_check(q, k, v, o, l, sample_rows(S, P, "zigzag", 192), what="ring s8192")
+    _sampled_check(q, k, v, o, l, sample_rows(S, P, "zigzag", 1024), what="ring s8192")
     o2, l2 = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "zigzag", "stepwise")
     check_ok()
     _sampled_check(q, k, v, o2, l2, sample_rows(S, P, "zigzag", 64, seed=2), what="ring s8192 stepwise")
