@@ -41,6 +41,9 @@
 // Warps: 0..7 softmax (two warpgroups), 8 TMA producer, 9 MMA issuer (one
 // thread), 10..11 spare (the third warpgroup gives registers to the softmax
 // ones with setmaxnreg).  Every mbarrier wait is bounded (as in the forward).
+// Both kernels launch their units heaviest first (the schedule's launch order:
+// units that see the most tiles start first, the lightest fill the last wave),
+// and take the sliding window as a template flag.
 #include <cuda.h>
 
 #include <vector>

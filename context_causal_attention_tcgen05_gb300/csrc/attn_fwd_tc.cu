@@ -29,6 +29,12 @@
 //               P is the A operand straight from TMEM (M=128 lanes, two bf16 per
 //               column); V is the B operand from shared memory (MN-major).
 // TMEM: S0/P0 cols 0..127, O0 128..255, S1/P1 256..383, O1 384..511.
+// Epilogue: each softmax warp normalises its 32 rows of O and, for bf16 output,
+// stages them in its query tile's Q buffer (free once every product completed)
+// in the 128-byte swizzled layout, then one lane writes them with TMA stores
+// (32-row boxes); fp32 output and warps holding rows past the group's end store
+// each row directly.  The sliding window is a template flag, so the unwindowed
+// kernel carries none of its terms.
 // Key/value tiles entirely masked for both query tiles are never loaded;
 // fully visible tiles skip the mask.  Every mbarrier wait is bounded; on
 // expiry the CTA records CP_ERR_DEVICE_TIMEOUT in the device error word,
