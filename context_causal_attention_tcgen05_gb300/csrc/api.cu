@@ -300,10 +300,25 @@ cp_status launch_fwd(const AttnArgs& a, Schedule& s, int32_t dtype, int64_t q_ro
   return launch_attn_fwd_simt(a, s, 0, st);
 }
 
+}  // namespace
+bool cpa::bwd_writes_bf16(int32_t dtype, int32_t D) { return dtype == CP_BF16 && D == 128; }
+
+bool cpa::grads_apart(const void* const* outs, const size_t* out_bytes, int n_out, const void* const* ins,
+                      const size_t* in_bytes, int n_in) {
+  for (int i = 0; i < n_out; ++i)
+    for (int j = 0; j < n_in; ++j) {
+      const char* o = static_cast<const char*>(outs[i]);
+      const char* x = static_cast<const char*>(ins[j]);
+      if (o && x && !(o + out_bytes[i] <= x || x + in_bytes[j] <= o)) return false;
+    }
+  return true;
+}
+namespace {
+
 cp_status launch_bwd(const BwdArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
                      int64_t k_rows, cudaStream_t st) {
   // The tensor-core backward is written for D = 128; other head sizes use the FFMA kernel.
-  if (dtype == CP_BF16 && a.D == 128) return launch_attn_bwd_tc(a, s, q_rows, k_rows, st);
+  if (bwd_writes_bf16(dtype, a.D)) return launch_attn_bwd_tc(a, s, q_rows, k_rows, st);
   return launch_attn_bwd_simt(a, s, dtype == CP_BF16, st);
 }
 
@@ -644,9 +659,19 @@ cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const v
   float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
   float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
   const int is_bf16 = dtype == CP_BF16;
-  CP_TRY(launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, st));
-  CP_TRY(launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, st));
-  CP_TRY(launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, st));
+  // The tensor-core kernels write every gradient row once, in bf16: no zeroing, no cast.
+  // Only into outputs that share no bytes with what the kernels still read.
+  const size_t qb = (size_t)Sq * Hq * D * dtype_size(dtype), kb = (size_t)Sk * Hkv * D * dtype_size(dtype);
+  const void* outs[3] = {dq, dk, dv};
+  const size_t ob[3] = {qb, kb, kb};
+  const void* ins[5] = {q, k, v, dout, lse};
+  const size_t ib[5] = {qb, kb, kb, qb, (size_t)Sq * Hq * 4};
+  const bool direct = bwd_writes_bf16(dtype, D) && Sq > 0 && Sk > 0 && grads_apart(outs, ob, 3, ins, ib, 5);
+  if (!direct) {
+    CP_TRY(launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, st));
+    CP_TRY(launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, st));
+    CP_TRY(launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, st));
+  }
   CP_TRY(launch_bwd_preprocess(out, dout, delta, Sq, Hq, D, (int32_t)Sq, is_bf16, st));
   Schedule* s = new Schedule;
   s->n_groups = 0;
@@ -663,12 +688,17 @@ cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const v
   a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
   a.window = m.window;
   a.err = device_error_word();
+  if (direct) {
+    a.dq_out = dq; a.dk_out = dk; a.dv_out = dv;
+  }
   cp_status stt = launch_bwd(a, *s, dtype, Sq, Sk, st);
   delete s;
   CP_TRY(stt);
-  CP_TRY(launch_cast_out(dq_acc, dq, Sq * Hq * D, is_bf16, st));
-  CP_TRY(launch_cast_out(dk_acc, dk, Sk * Hkv * D, is_bf16, st));
-  CP_TRY(launch_cast_out(dv_acc, dv, Sk * Hkv * D, is_bf16, st));
+  if (!direct) {
+    CP_TRY(launch_cast_out(dq_acc, dq, Sq * Hq * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dk_acc, dk, Sk * Hkv * D, is_bf16, st));
+    CP_TRY(launch_cast_out(dv_acc, dv, Sk * Hkv * D, is_bf16, st));
+  }
   return CP_OK;
 }
 
@@ -1007,8 +1037,22 @@ cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, con
   float* dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
   float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
   float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
-  CP_TRY(launch_zero(dq_acc, (size_t)S * Hq * D * 4, st));
+  // The tensor-core kernels write every gradient row once, in bf16: no zeroing, no cast.
+  // Reordered: into the (then unused) fp32 accumulator space, since the dQ kernel still
+  // reads the staged k/v after the dK/dV kernel is done.  In place: into the outputs,
+  // if they share no bytes with what the kernels read.
+  const size_t qbytes = (size_t)S * Hq * D * es, kbytes = (size_t)S * Hkv * D * es;
+  const void* outs[3] = {dq, dk, dv};
+  const size_t ob[3] = {qbytes, kbytes, kbytes};
+  const void* ins[5] = {q, k, v, dout, lse};
+  const size_t ib[5] = {qbytes, kbytes, kbytes, qbytes, (size_t)S * Hq * 4};
+  const bool direct = bwd_writes_bf16(dtype, D) && (moved || grads_apart(outs, ob, 3, ins, ib, 5));
+  if (!direct) CP_TRY(launch_zero(dq_acc, (size_t)S * Hq * D * 4, st));
   CP_TRY(launch_bwd_preprocess(o_re, do_re, delta, S, Hq, D, (int32_t)S, is_bf16, st));
+  // where the gradients land in rank order (then restored when the layout moved)
+  void* dq_c = !moved ? dq : direct ? static_cast<void*>(dq_acc) : ws_at(workspace, w.q);
+  void* dk_c = !moved ? dk : direct ? static_cast<void*>(dk_acc) : ws_at(workspace, w.k);
+  void* dv_c = !moved ? dv : direct ? static_cast<void*>(dv_acc) : ws_at(workspace, w.v);
   Schedule* s = new Schedule;
   build_ring_bwd_schedule(*s, S, P, layout, 1);
   BwdArgs a;
@@ -1021,25 +1065,22 @@ cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, con
   a.scale_log2 = a.scale * 1.4426950408889634f;
   a.causal = 1; a.cu_seqlens = cu_seqlens; a.n_docs = cu_seqlens ? n_docs : 0;
   a.err = device_error_word();
+  if (direct) {
+    a.dq_out = dq_c; a.dk_out = dk_c; a.dv_out = dv_c;
+  }
   cp_status stt = launch_bwd(a, *s, dtype, S, S, st);
   delete s;
   CP_TRY(stt);
-  if (moved) {
-    // q/k/v staging buffers are free now: cast into them, then restore the order.
-    void* dq_c = ws_at(workspace, w.q);
-    void* dk_c = ws_at(workspace, w.k);
-    void* dv_c = ws_at(workspace, w.v);
+  if (!direct) {
     CP_TRY(launch_cast_out(dq_acc, dq_c, S * Hq * D, is_bf16, st));
     CP_TRY(launch_cast_out(dk_acc, dk_c, S * Hkv * D, is_bf16, st));
     CP_TRY(launch_cast_out(dv_acc, dv_c, S * Hkv * D, is_bf16, st));
+  }
+  if (moved) {  // back to sequence order
     GatherJob jobs[3] = {{back_kind, dq_c, dq, S, (int64_t)Hq * D * (int64_t)es, P},
                          {back_kind, dk_c, dk, S, (int64_t)Hkv * D * (int64_t)es, P},
                          {back_kind, dv_c, dv, S, (int64_t)Hkv * D * (int64_t)es, P}};
     CP_TRY(launch_row_gather_batch(jobs, 3, st));
-  } else {
-    CP_TRY(launch_cast_out(dq_acc, dq, S * Hq * D, is_bf16, st));
-    CP_TRY(launch_cast_out(dk_acc, dk, S * Hkv * D, is_bf16, st));
-    CP_TRY(launch_cast_out(dv_acc, dv, S * Hkv * D, is_bf16, st));
   }
   return CP_OK;
 }

@@ -59,6 +59,18 @@ constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSoftmaxThreads = 256;
+
+// 32 fp32 accumulator columns (raw TMEM words) times mul, rounded to bf16, as
+// four 16-byte stores (dst 16-byte aligned).
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&rr)[32], float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v4 = 0; v4 < 4; ++v4)
+    d4[v4] = make_uint4(ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 0]) * mul, __uint_as_float(rr[8 * v4 + 1]) * mul),
+                        ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 2]) * mul, __uint_as_float(rr[8 * v4 + 3]) * mul),
+                        ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 4]) * mul, __uint_as_float(rr[8 * v4 + 5]) * mul),
+                        ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 6]) * mul, __uint_as_float(rr[8 * v4 + 7]) * mul));
+}
 // Register split (launch: 384 x 168 = 64512): the TMA/MMA warpgroup drops to 88, the
 // two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
 constexpr int kRegsLow = 88;
@@ -541,6 +553,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
       const bool valid = r < nk_tile;
       const int64_t krow = (int64_t)(k_row0 + r) * a.k_ld + (int64_t)hk * D;
       float* dst = (wg == 0 ? a.dv_acc : a.dk_acc) + krow;  // warpgroup 0: dV, 1: dK
+      void* out_bf = wg == 0 ? a.dv_out : a.dk_out;
+      __nv_bfloat16* dst_bf = out_bf ? static_cast<__nv_bfloat16*>(out_bf) + krow : nullptr;
       const float mul = wg == 0 ? 1.f : a.scale;
       const uint32_t col0 = wg == 0 ? 256 : 384;
 #pragma unroll
@@ -553,7 +567,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (valid) {
+        if (valid && dst_bf) {
+          store_row_bf16(dst_bf + ch * 32, rr, mul);
+        } else if (valid) {
           float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)
@@ -958,7 +974,9 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     if (ok) ok = wait_all(&bars->done, 0, abort_flag, a.err);
     if (ok) {
       ptx::tc_fence_after();
-      float* dst = a.dq_acc + (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
+      const int64_t qrow = (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
+      float* dst = a.dq_acc + qrow;
+      __nv_bfloat16* dst_bf = a.dq_out ? static_cast<__nv_bfloat16*>(a.dq_out) + qrow : nullptr;
 #pragma unroll
       for (int ch = w * 2; ch < w * 2 + 2; ++ch) {  // 64 columns per warpgroup
         uint32_t rr[32];
@@ -969,7 +987,9 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (row_valid) {
+        if (row_valid && dst_bf) {
+          store_row_bf16(dst_bf + ch * 32, rr, a.scale);
+        } else if (row_valid) {
           float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4)

@@ -91,6 +91,12 @@ struct BwdArgs {
   float* dq_acc;       // [rows_q, Hq, D] fp32
   float* dk_acc;       // [rows_k, Hkv, D] fp32
   float* dv_acc;       // [rows_k, Hkv, D] fp32
+  // bf16 outputs written directly by the tensor-core kernels (same layout as the
+  // accumulators; every row is written once, so no zeroing or cast pass); NULL:
+  // the fp32 accumulators above are written instead.
+  void* dq_out;
+  void* dk_out;
+  void* dv_out;
   int64_t q_ld, k_ld;
   int32_t Hq, Hkv, D;
   int32_t lse_ld;
@@ -173,6 +179,14 @@ enum GatherKind : int {
   kZigzagReorderCols = 7,  // the zigzag maps on the columns of an lse [H, S] fp32 array,
   kZigzagRestoreCols = 8,  // as 16-byte runs (needs S/(2P) % 4 == 0)
 };
+
+// True when the backward runs on the tensor-core kernels (bf16, D = 128), which
+// write bf16 gradients directly (BwdArgs::dq_out etc.).
+bool bwd_writes_bf16(int32_t dtype, int32_t D);
+// True when none of the n_out output ranges overlaps any of the n_in input ranges
+// (NULL entries are skipped).
+bool grads_apart(const void* const* outs, const size_t* out_bytes, int n_out, const void* const* ins,
+                 const size_t* in_bytes, int n_in);
 
 // Fills group tile prefix sums for a query tile height; returns total units (tiles x heads).
 // Clears the launch order table.

@@ -122,10 +122,19 @@ extern "C" cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, con
   float* dv_acc = reinterpret_cast<float*>(b + off_dv);
   const int is_bf16 = dtype == CP_BF16;
 
-  // The array keeps the previous call's values: clear the accumulators first.
-  if ((st = launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, s)) != CP_OK) return st;
-  if ((st = launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, s)) != CP_OK) return st;
-  if ((st = launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, s)) != CP_OK) return st;
+  // The tensor-core kernels write every gradient row once, in bf16 (no accumulators);
+  // otherwise the array keeps the previous call's values: clear the accumulators first.
+  const size_t qb = (size_t)Sq * Hq * D * 2, kb = (size_t)Sk * Hkv * D * 2;  // bf16 when direct
+  const void* outs[3] = {dq, dk, dv};
+  const size_t ob[3] = {qb, kb, kb};
+  const void* ins[5] = {q, k, v, dout, lse};
+  const size_t ib[5] = {qb, kb, kb, qb, (size_t)Sq * Hq * 4};
+  const bool direct = bwd_writes_bf16(dtype, D) && Sq > 0 && Sk > 0 && grads_apart(outs, ob, 3, ins, ib, 5);
+  if (!direct) {
+    if ((st = launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, s)) != CP_OK) return st;
+    if ((st = launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, s)) != CP_OK) return st;
+    if ((st = launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, s)) != CP_OK) return st;
+  }
   if ((st = launch_bwd_preprocess(out, dout, delta, Sq, Hq, D, (int32_t)Sq, is_bf16, s)) != CP_OK)
     return st;
 
@@ -154,9 +163,12 @@ extern "C" cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, con
   a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
   a.window = m.window;
   a.err = device_error_word();
-  st = (is_bf16 && D == 128) ? launch_attn_bwd_tc(a, sched, Sq, Sk, s)
-                             : launch_attn_bwd_simt(a, sched, is_bf16, s);
-  if (st != CP_OK) return st;
+  if (direct) {
+    a.dq_out = dq; a.dk_out = dk; a.dv_out = dv;
+  }
+  st = bwd_writes_bf16(dtype, D) ? launch_attn_bwd_tc(a, sched, Sq, Sk, s)
+                                 : launch_attn_bwd_simt(a, sched, is_bf16, s);
+  if (st != CP_OK || direct) return st;
   if ((st = launch_cast_out(dq_acc, dq, Sq * Hq * D, is_bf16, s)) != CP_OK) return st;
   if ((st = launch_cast_out(dk_acc, dk, Sk * Hkv * D, is_bf16, s)) != CP_OK) return st;
   return launch_cast_out(dv_acc, dv, Sk * Hkv * D, is_bf16, s);

@@ -268,3 +268,31 @@ def test_batched_ring_permutes_bitexact(S, Hq, Hkv, D, P, dtype):
         out2, none = cpa.cp_ring_restore(kr, None, P, layout)
         assert none is None and torch.equal(out2.cpu(), k)
     check_ok()
+
+
+def test_block_bwd_gradient_aliasing_an_input():
+    # dq written over dout's storage: the kernels still read dout, so the library
+    # accumulates in fp32 and casts after them (the direct bf16 path needs disjoint
+    # buffers); the result equals the ordinary call bit for bit
+    import ctypes
+    Sq = Sk = 256
+    Hq, Hkv, D = 4, 2, 128
+    g = torch.Generator().manual_seed(51)
+    q, k, v, do = (torch.randn(S, H, D, generator=g).to(torch.bfloat16).cuda()
+                   for S, H in ((Sq, Hq), (Sk, Hkv), (Sk, Hkv), (Sq, Hq)))
+    o, l = cpa.cp_attn_block_fwd(q, k, v, True)
+    dq_ref, dk_ref, dv_ref = cpa.cp_attn_block_bwd(q, k, v, o, do, l, True)
+    buf = do.clone()  # dout and dq share this storage
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(cpa.cp_workspace_size("block_bwd", Sq, Hq, Hkv, D, q.dtype, 1), dtype=torch.uint8,
+                     device="cuda")
+    m = cpa._mask(True, 0, 0, 1, 1, None, 0)
+    lib = cpa.load_library()
+    st = lib.cp_attn_block_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), buf.data_ptr(),
+                               l.data_ptr(), Sq, Sk, Hq, Hkv, D, cpa.CP_BF16, ctypes.byref(m), 0.0,
+                               buf.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                               torch.cuda.current_stream().cuda_stream)
+    assert st == 0, cpa.cp_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(buf, dq_ref) and torch.equal(dk, dk_ref) and torch.equal(dv, dv_ref)
+    check_ok()
