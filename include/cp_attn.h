@@ -127,7 +127,10 @@ CP_API cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, 
  * sum(dout * out) given the FINAL out and lse of the rows (for a ring, the
  * merged ones), i.e. P = exp(s - lse), dS = P (dP - rowsum(dout*out)).
  *   dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype` (overwritten; dk/dv are summed
- *   over the Hq/Hkv query heads of each key/value head).
+ *   over the Hq/Hkv query heads of each key/value head).  For bf16 with D = 128
+ *   the tensor-core kernels write them directly; gradients that share storage
+ *   with an input are still correct (then fp32 accumulators in the workspace
+ *   are cast after the kernels, as on the FFMA path).
  *   workspace: >= cp_workspace_size(CP_OP_BLOCK_BWD, ...) bytes (fp32 accumulators). */
 CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
                             const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
