@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcp_attn.
 
 __all__ = [
     "CpAttnError", "load_library", "library_path", "header_functions",
-    "cp_attn_block_fwd", "cp_attn_block_bwd", "cp_attn_block_bwd_noalloc", "cp_lse_merge",
+    "cp_attn_block_fwd", "cp_attn_block_bwd", "cp_attn_block_bwd_typed", "cp_attn_block_bwd_noalloc",
+    "cp_lse_merge",
     "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
     "cp_lse_reorder", "cp_ring_reorder_qkv", "cp_ring_restore",
@@ -52,7 +53,10 @@ _SIGS = {
     "cp_attn_block_fwd": [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32,
                           ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p],
     "cp_attn_block_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32,
-                          _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
+                          _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_size,
+                          _c_p],
+    "cp_attn_block_bwd_typed": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32, _c_i32,
+                                _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_attn_block_bwd_noalloc": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i32, _c_i32,
                                   _c_i32, _c_i32, ctypes.POINTER(cp_mask), _c_f32, _c_p, _c_p, _c_p, _c_p],
     "cp_lse_merge": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_p],
@@ -205,14 +209,38 @@ def cp_attn_block_fwd(q, k, v, causal=True, q_offset=0, k_offset=0, q_stride=1, 
 
 
 def cp_attn_block_bwd(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0, q_stride=1,
-                      k_stride=1, cu_seqlens=None, scale=0.0, stream=None, window=0):
-    """(dq, dk, dv) of one block pair given the final out and lse."""
+                      k_stride=1, cu_seqlens=None, scale=0.0, dq_acc=None, dk_acc=None, dv_acc=None,
+                      accumulate=False, workspace=None, stream=None, window=0):
+    """fp32 (dq_acc, dk_acc, dv_acc) of one block pair given the FINAL out and lse:
+    overwritten, or (accumulate=True) this pair's gradients added to what they hold."""
+    Sq, Hq, D = q.shape
+    Sk, Hkv, _ = k.shape
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq_acc = torch.empty(Sq, Hq, D, **f32) if dq_acc is None else dq_acc
+    dk_acc = torch.empty(Sk, Hkv, D, **f32) if dk_acc is None else dk_acc
+    dv_acc = torch.empty(Sk, Hkv, D, **f32) if dv_acc is None else dv_acc
+    for t in (dq_acc, dk_acc, dv_acc):
+        if t.dtype != torch.float32:
+            raise TypeError("the accumulating block backward takes fp32 gradient buffers")
+    if workspace is None:
+        workspace = _workspace(cp_workspace_size("block_bwd", max(Sq, Sk), Hq, Hkv, D, q.dtype, 1), q.device)
+    m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens, window)
+    _check("cp_attn_block_bwd", load_library().cp_attn_block_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
+        ctypes.byref(m), float(scale), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), int(bool(accumulate)),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq_acc, dk_acc, dv_acc
+
+
+def cp_attn_block_bwd_typed(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0, q_stride=1,
+                            k_stride=1, cu_seqlens=None, scale=0.0, stream=None, window=0):
+    """(dq, dk, dv) in the input dtype of one block pair given the final out and lse."""
     Sq, Hq, D = q.shape
     Sk, Hkv, _ = k.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = _workspace(cp_workspace_size("block_bwd", max(Sq, Sk), Hq, Hkv, D, q.dtype, 1), q.device)
     m = _mask(causal, q_offset, k_offset, q_stride, k_stride, cu_seqlens, window)
-    _check("cp_attn_block_bwd", load_library().cp_attn_block_bwd(
+    _check("cp_attn_block_bwd_typed", load_library().cp_attn_block_bwd_typed(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), Sq, Sk, Hq, Hkv, D, _dt(q),
         ctypes.byref(m), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
         _stream(stream)))
@@ -222,9 +250,9 @@ def cp_attn_block_bwd(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset
 def cp_attn_block_bwd_noalloc(q, k, v, out, dout, lse, causal=True, q_offset=0, k_offset=0,
                               q_stride=1, k_stride=1, cu_seqlens=None, scale=0.0, dq=None, dk=None,
                               dv=None, stream=None, window=0):
-    """cp_attn_block_bwd without a workspace: the library uses its built-in
-    32 MiB scratch array and allocates nothing (outputs are allocated here
-    unless passed in)."""
+    """cp_attn_block_bwd_typed without a workspace: the library uses its built-in
+    32 MiB scratch array and allocates no device memory (outputs are allocated
+    here unless passed in)."""
     Sq, Hq, D = q.shape
     Sk, Hkv, _ = k.shape
     dq = torch.empty_like(q) if dq is None else dq

@@ -560,6 +560,85 @@ cp_status check_ring_args(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t
 
 }  // namespace
 
+cp_status cpa::check_block_args(int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                                const cp_mask* mask, cp_mask* m) {
+  CP_TRY(check_common(Hq, Hkv, D, dtype));
+  CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
+  CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
+             CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
+  *m = cp_mask{1, 0, 0, 1, 1, nullptr, 0, 0};
+  if (mask) *m = *mask;
+  CP_REQUIRE(m->q_stride >= 1 && m->k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
+  CP_REQUIRE(m->window >= 0, CP_ERR_INVALID_ARG, "mask window must be >= 0");
+  CP_REQUIRE(m->window == 0 || m->causal, CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
+  // Offsets and strides are bounded before any product is formed, so the
+  // position arithmetic below cannot overflow int64.
+  CP_REQUIRE(fits_i32(m->q_offset) && fits_i32(m->k_offset) && m->q_stride <= INT32_MAX &&
+                 m->k_stride <= INT32_MAX,
+             CP_ERR_UNSUPPORTED, "positions must fit in int32");
+  CP_REQUIRE(fits_i32(m->q_offset + m->q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
+                 fits_i32(m->k_offset + m->k_stride * (Sk > 0 ? Sk - 1 : 0)),
+             CP_ERR_UNSUPPORTED, "positions must fit in int32");
+  CP_REQUIRE(!m->cu_seqlens || m->n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  return CP_OK;
+}
+
+cp_status cpa::block_bwd_run(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                             const float* lse, int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t D,
+                             int32_t dtype, const cp_mask& m, float scale, const BlockBwdOut& o, float* delta,
+                             cudaStream_t st) {
+  const int is_bf16 = dtype == CP_BF16;
+  const bool tc = bwd_writes_bf16(dtype, D);
+  bool direct = false;  // typed bf16 gradients written by the tensor-core kernels themselves
+  if (o.typed) {
+    // Every gradient row is written once, in bf16, with no zeroing or cast pass, but
+    // only into outputs that share no bytes with what the kernels still read.
+    const size_t qb = (size_t)Sq * Hq * D * dtype_size(dtype), kb = (size_t)Sk * Hkv * D * dtype_size(dtype);
+    const void* outs[3] = {o.dq, o.dk, o.dv};
+    const size_t ob[3] = {qb, kb, kb};
+    const void* ins[5] = {q, k, v, dout, lse};
+    const size_t ib[5] = {qb, kb, kb, qb, (size_t)Sq * Hq * 4};
+    direct = tc && Sq > 0 && Sk > 0 && grads_apart(outs, ob, 3, ins, ib, 5);
+    if (!direct) {
+      CP_TRY(launch_zero(o.dq_acc, (size_t)Sq * Hq * D * 4, st));
+      CP_TRY(launch_zero(o.dk_acc, (size_t)Sk * Hkv * D * 4, st));
+      CP_TRY(launch_zero(o.dv_acc, (size_t)Sk * Hkv * D * 4, st));
+    }
+  } else if (!tc && !o.accumulate) {
+    // the FFMA kernel adds dQ atomically (dK/dV rows are stored once): start it at zero
+    CP_TRY(launch_zero(o.dq_acc, (size_t)Sq * Hq * D * 4, st));
+  }
+  CP_TRY(launch_bwd_preprocess(out, dout, delta, Sq, Hq, D, (int32_t)Sq, is_bf16, st));
+  Schedule* s = new Schedule;
+  s->n_groups = 0;
+  s->n_segs = 0;
+  add_group(*s, Piece{0, (int32_t)Sk, (int32_t)m.k_offset, (int32_t)m.k_stride});
+  if (Sq > 0) add_seg(*s, Piece{0, (int32_t)Sq, (int32_t)m.q_offset, (int32_t)m.q_stride});
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
+  a.dq_acc = o.dq_acc; a.dk_acc = o.dk_acc; a.dv_acc = o.dv_acc;
+  a.q_ld = (int64_t)Hq * D; a.k_ld = (int64_t)Hkv * D;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)Sq;
+  a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
+  a.window = m.window;
+  a.accumulate = o.typed ? 0 : o.accumulate;
+  a.err = device_error_word();
+  if (direct) {
+    a.dq_out = o.dq; a.dk_out = o.dk; a.dv_out = o.dv;
+  }
+  cp_status stt = launch_bwd(a, *s, dtype, Sq, Sk, st);
+  delete s;
+  CP_TRY(stt);
+  if (o.typed && !direct) {
+    CP_TRY(launch_cast_out(o.dq_acc, o.dq, Sq * Hq * D, is_bf16, st));
+    CP_TRY(launch_cast_out(o.dk_acc, o.dk, Sk * Hkv * D, is_bf16, st));
+    CP_TRY(launch_cast_out(o.dv_acc, o.dv, Sk * Hkv * D, is_bf16, st));
+  }
+  return CP_OK;
+}
+
 // ====================================================================== C ABI
 extern "C" {
 
@@ -585,20 +664,8 @@ const char* cp_status_string(int32_t st) {
 cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t Sq, int64_t Sk,
                             int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask,
                             float scale, void* out, float* lse, void* stream) {
-  CP_TRY(check_common(Hq, Hkv, D, dtype));
-  CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
-  CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
-             CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
-  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0, 0};
-  if (mask) m = *mask;
-  CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
-  CP_REQUIRE(m.window >= 0, CP_ERR_INVALID_ARG, "mask window must be >= 0");
-  CP_REQUIRE(m.window == 0 || m.causal, CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
-  CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
-                 fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
-                 fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
-             CP_ERR_UNSUPPORTED, "positions must fit in int32");
-  CP_REQUIRE(!m.cu_seqlens || m.n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
+  cp_mask m;
+  CP_TRY(check_block_args(Sq, Sk, Hq, Hkv, D, dtype, mask, &m));
   if (Sq == 0) return CP_OK;
   CP_CHECK_T(q, "q", false);
   CP_CHECK_T(k, "k", Sk == 0);
@@ -620,29 +687,10 @@ cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, int64_t
   return st;
 }
 
-cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
-                            const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
-                            int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
-                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-                            void* stream) {
-  CP_TRY(check_common(Hq, Hkv, D, dtype));
-  CP_REQUIRE(Sq >= 0 && Sk >= 0, CP_ERR_INVALID_ARG, "Sq and Sk must be >= 0");
-  CP_REQUIRE(Sq * (int64_t)Hq < (int64_t)INT32_MAX && Sk * (int64_t)Hkv < (int64_t)INT32_MAX,
-             CP_ERR_UNSUPPORTED, "S*H must be < 2^31");
-  cp_mask m = {1, 0, 0, 1, 1, nullptr, 0, 0};
-  if (mask) m = *mask;
-  CP_REQUIRE(m.q_stride >= 1 && m.k_stride >= 1, CP_ERR_INVALID_ARG, "mask strides must be >= 1");
-  CP_REQUIRE(m.window >= 0, CP_ERR_INVALID_ARG, "mask window must be >= 0");
-  CP_REQUIRE(m.window == 0 || m.causal, CP_ERR_UNSUPPORTED, "a sliding window needs the causal rule");
-  CP_REQUIRE(fits_i32(m.q_offset) && fits_i32(m.k_offset) &&
-                 fits_i32(m.q_offset + m.q_stride * (Sq > 0 ? Sq - 1 : 0)) &&
-                 fits_i32(m.k_offset + m.k_stride * (Sk > 0 ? Sk - 1 : 0)),
-             CP_ERR_UNSUPPORTED, "positions must fit in int32");
-  CP_REQUIRE(!m.cu_seqlens || m.n_docs >= 1, CP_ERR_INVALID_ARG, "n_docs must be >= 1 with cu_seqlens");
-  if (Sq == 0 && Sk == 0) return CP_OK;
-  BlockBwdWs w = block_bwd_ws(Sq, Sk, Hq, Hkv, D);
-  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for block bwd");
-  CP_CHECK_T(workspace, "workspace", false);
+// Pointer checks shared by both block backward forms (q side when Sq > 0, k side when Sk > 0).
+static cp_status check_block_bwd_ptrs(const void* q, const void* k, const void* v, const void* out,
+                                      const void* dout, const float* lse, const void* dq, const void* dk,
+                                      const void* dv, int64_t Sq, int64_t Sk) {
   CP_CHECK_T(q, "q", Sq == 0);
   CP_CHECK_T(out, "out", Sq == 0);
   CP_CHECK_T(dout, "dout", Sq == 0);
@@ -652,54 +700,72 @@ cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const v
   CP_CHECK_T(v, "v", Sk == 0);
   CP_CHECK_T(dk, "dk", Sk == 0);
   CP_CHECK_T(dv, "dv", Sk == 0);
-  if (scale == 0.f) scale = 1.0f / sqrtf((float)D);
-  cudaStream_t st = (cudaStream_t)stream;
-  float* delta = reinterpret_cast<float*>(ws_at(workspace, w.delta));
-  float* dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
-  float* dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
-  float* dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
-  const int is_bf16 = dtype == CP_BF16;
-  // The tensor-core kernels write every gradient row once, in bf16: no zeroing, no cast.
-  // Only into outputs that share no bytes with what the kernels still read.
-  const size_t qb = (size_t)Sq * Hq * D * dtype_size(dtype), kb = (size_t)Sk * Hkv * D * dtype_size(dtype);
-  const void* outs[3] = {dq, dk, dv};
-  const size_t ob[3] = {qb, kb, kb};
-  const void* ins[5] = {q, k, v, dout, lse};
-  const size_t ib[5] = {qb, kb, kb, qb, (size_t)Sq * Hq * 4};
-  const bool direct = bwd_writes_bf16(dtype, D) && Sq > 0 && Sk > 0 && grads_apart(outs, ob, 3, ins, ib, 5);
-  if (!direct) {
-    CP_TRY(launch_zero(dq_acc, (size_t)Sq * Hq * D * 4, st));
-    CP_TRY(launch_zero(dk_acc, (size_t)Sk * Hkv * D * 4, st));
-    CP_TRY(launch_zero(dv_acc, (size_t)Sk * Hkv * D * 4, st));
-  }
-  CP_TRY(launch_bwd_preprocess(out, dout, delta, Sq, Hq, D, (int32_t)Sq, is_bf16, st));
-  Schedule* s = new Schedule;
-  s->n_groups = 0;
-  s->n_segs = 0;
-  add_group(*s, Piece{0, (int32_t)Sk, (int32_t)m.k_offset, (int32_t)m.k_stride});
-  if (Sq > 0) add_seg(*s, Piece{0, (int32_t)Sq, (int32_t)m.q_offset, (int32_t)m.q_stride});
-  BwdArgs a;
-  memset(&a, 0, sizeof(a));
-  a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
-  a.dq_acc = dq_acc; a.dk_acc = dk_acc; a.dv_acc = dv_acc;
-  a.q_ld = (int64_t)Hq * D; a.k_ld = (int64_t)Hkv * D;
-  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.lse_ld = (int32_t)Sq;
-  a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
-  a.causal = m.causal; a.cu_seqlens = m.cu_seqlens; a.n_docs = m.cu_seqlens ? m.n_docs : 0;
-  a.window = m.window;
-  a.err = device_error_word();
-  if (direct) {
-    a.dq_out = dq; a.dk_out = dk; a.dv_out = dv;
-  }
-  cp_status stt = launch_bwd(a, *s, dtype, Sq, Sk, st);
-  delete s;
-  CP_TRY(stt);
-  if (!direct) {
-    CP_TRY(launch_cast_out(dq_acc, dq, Sq * Hq * D, is_bf16, st));
-    CP_TRY(launch_cast_out(dk_acc, dk, Sk * Hkv * D, is_bf16, st));
-    CP_TRY(launch_cast_out(dv_acc, dv, Sk * Hkv * D, is_bf16, st));
-  }
   return CP_OK;
+}
+
+cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
+                            float* dq_acc, float* dk_acc, float* dv_acc, int32_t accumulate,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  cp_mask m;
+  CP_TRY(check_block_args(Sq, Sk, Hq, Hkv, D, dtype, mask, &m));
+  CP_REQUIRE(accumulate == 0 || accumulate == 1, CP_ERR_INVALID_ARG, "accumulate must be 0 or 1");
+  if (Sq == 0 && Sk == 0) return CP_OK;
+  const size_t delta_bytes = align_up((size_t)Sq * Hq * 4);
+  CP_REQUIRE(Sq == 0 || (workspace && ws_bytes >= delta_bytes), CP_ERR_WORKSPACE,
+             "workspace too small for the block backward (4*Hq*Sq bytes of Delta)");
+  if (Sq > 0) CP_CHECK_T(workspace, "workspace", false);
+  CP_TRY(check_block_bwd_ptrs(q, k, v, out, dout, lse, dq_acc, dk_acc, dv_acc, Sq, Sk));
+  // The fp32 outputs are read back when accumulating and written while the kernels
+  // still read the inputs: they may overlap neither an input nor each other.
+  const size_t es = dtype_size(dtype);
+  const size_t qb = (size_t)Sq * Hq * D * es, kb = (size_t)Sk * Hkv * D * es;
+  const size_t qa = (size_t)Sq * Hq * D * 4, ka = (size_t)Sk * Hkv * D * 4;
+  const void* outs[3] = {dq_acc, dk_acc, dv_acc};
+  const size_t ob[3] = {qa, ka, ka};
+  const void* ins[7] = {q, k, v, out, dout, lse, Sq > 0 ? workspace : nullptr};
+  const size_t ib[7] = {qb, kb, kb, qb, qb, (size_t)Sq * Hq * 4, delta_bytes};
+  CP_REQUIRE(grads_apart(outs, ob, 3, ins, ib, 7) && grads_apart(outs, ob, 1, outs + 1, ob + 1, 2) &&
+                 grads_apart(outs + 1, ob + 1, 1, outs + 2, ob + 2, 1),
+             CP_ERR_INVALID_ARG,
+             "dq_acc, dk_acc and dv_acc must not overlap an input, the workspace or each other");
+  if (scale == 0.f) scale = 1.0f / sqrtf((float)D);
+  BlockBwdOut o;
+  memset(&o, 0, sizeof(o));
+  o.typed = false;
+  o.dq_acc = dq_acc;
+  o.dk_acc = dk_acc;
+  o.dv_acc = dv_acc;
+  o.accumulate = accumulate;
+  return block_bwd_run(q, k, v, out, dout, lse, Sq, Sk, Hq, Hkv, D, dtype, m, scale, o,
+                       static_cast<float*>(workspace), (cudaStream_t)stream);
+}
+
+cp_status cp_attn_block_bwd_typed(const void* q, const void* k, const void* v, const void* out,
+                                  const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
+                                  void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                  void* stream) {
+  cp_mask m;
+  CP_TRY(check_block_args(Sq, Sk, Hq, Hkv, D, dtype, mask, &m));
+  if (Sq == 0 && Sk == 0) return CP_OK;
+  BlockBwdWs w = block_bwd_ws(Sq, Sk, Hq, Hkv, D);
+  CP_REQUIRE(workspace && ws_bytes >= w.total, CP_ERR_WORKSPACE, "workspace too small for block bwd");
+  CP_CHECK_T(workspace, "workspace", false);
+  CP_TRY(check_block_bwd_ptrs(q, k, v, out, dout, lse, dq, dk, dv, Sq, Sk));
+  if (scale == 0.f) scale = 1.0f / sqrtf((float)D);
+  BlockBwdOut o;
+  o.typed = true;
+  o.dq = dq;
+  o.dk = dk;
+  o.dv = dv;
+  o.dq_acc = reinterpret_cast<float*>(ws_at(workspace, w.dq));
+  o.dk_acc = reinterpret_cast<float*>(ws_at(workspace, w.dk));
+  o.dv_acc = reinterpret_cast<float*>(ws_at(workspace, w.dv));
+  o.accumulate = 0;
+  return block_bwd_run(q, k, v, out, dout, lse, Sq, Sk, Hq, Hkv, D, dtype, m, scale, o,
+                       reinterpret_cast<float*>(ws_at(workspace, w.delta)), (cudaStream_t)stream);
 }
 
 cp_status cp_lse_merge(const void* o1, const float* lse1, const void* o2, const float* lse2,

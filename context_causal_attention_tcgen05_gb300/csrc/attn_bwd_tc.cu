@@ -71,6 +71,24 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
                         ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 4]) * mul, __uint_as_float(rr[8 * v4 + 5]) * mul),
                         ptx::pack_bf16x2(__uint_as_float(rr[8 * v4 + 6]) * mul, __uint_as_float(rr[8 * v4 + 7]) * mul));
 }
+// 32 fp32 accumulator columns times mul into 32 fp32 values (dst 16-byte aligned):
+// overwritten, or added to what dst holds when `add` (the accumulating form).
+__device__ __forceinline__ void store_row_f32(float* dst, const uint32_t (&rr)[32], float mul, int add) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int v4 = 0; v4 < 8; ++v4) {
+    float4 x = make_float4(__uint_as_float(rr[4 * v4]) * mul, __uint_as_float(rr[4 * v4 + 1]) * mul,
+                           __uint_as_float(rr[4 * v4 + 2]) * mul, __uint_as_float(rr[4 * v4 + 3]) * mul);
+    if (add) {
+      const float4 o = d4[v4];
+      x.x += o.x;
+      x.y += o.y;
+      x.z += o.z;
+      x.w += o.w;
+    }
+    d4[v4] = x;
+  }
+}
 // Register split (launch: 384 x 168 = 64512): the TMA/MMA warpgroup drops to 88, the
 // two softmax warpgroups rise to 208: 128*88 + 256*208 = 64512.
 constexpr int kRegsLow = 88;
@@ -570,11 +588,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         if (valid && dst_bf) {
           store_row_bf16(dst_bf + ch * 32, rr, mul);
         } else if (valid) {
-          float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            d4[v4] = make_float4(__uint_as_float(rr[4 * v4]) * mul, __uint_as_float(rr[4 * v4 + 1]) * mul,
-                                 __uint_as_float(rr[4 * v4 + 2]) * mul, __uint_as_float(rr[4 * v4 + 3]) * mul);
+          store_row_f32(dst + ch * 32, rr, mul, a.accumulate);
         }
       }
     }
@@ -990,11 +1004,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
         if (row_valid && dst_bf) {
           store_row_bf16(dst_bf + ch * 32, rr, a.scale);
         } else if (row_valid) {
-          float4* d4 = reinterpret_cast<float4*>(dst + ch * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            d4[v4] = make_float4(__uint_as_float(rr[4 * v4]) * a.scale, __uint_as_float(rr[4 * v4 + 1]) * a.scale,
-                                 __uint_as_float(rr[4 * v4 + 2]) * a.scale, __uint_as_float(rr[4 * v4 + 3]) * a.scale);
+          store_row_f32(dst + ch * 32, rr, a.scale, a.accumulate);
         }
       }
     }

@@ -16,7 +16,8 @@
 // one CTA = one tile of 32 keys of one key/value head, looping over the G
 // query heads that read it and every query row of every query segment that
 // sees it.  dK and dV of the tile accumulate in shared memory and are stored
-// once; dQ accumulates in an fp32 buffer with atomic adds.
+// once (or added to the fp32 outputs in the accumulating form); dQ accumulates
+// in an fp32 buffer with atomic adds (zeroed by the caller unless accumulating).
 #include <math.h>
 
 #include "common.cuh"
@@ -269,8 +270,8 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(BwdArgs a, Schedule 
     int jj = j0 + r;
     if (jj < kg.nq) {
       int64_t off = (int64_t)(kg.q_row0 + jj) * a.k_ld + (int64_t)hk * D + d;
-      a.dk_acc[off] = dks[r * Dp + d];
-      a.dv_acc[off] = dvs[r * Dp + d];
+      a.dk_acc[off] = dks[r * Dp + d] + (a.accumulate ? a.dk_acc[off] : 0.f);
+      a.dv_acc[off] = dvs[r * Dp + d] + (a.accumulate ? a.dv_acc[off] : 0.f);
     }
   }
 }

@@ -107,6 +107,8 @@ struct BwdArgs {
   int32_t* err;
   int32_t total_units;
   int32_t window;      // sliding window (causal only): pos_q - pos_k < window; 0 = none
+  int32_t accumulate;  // fp32 outputs: add into the values already there (each row is still
+                       // written by one CTA, so no atomics); 0 = overwrite
 };
 
 // Device error codes written into the error word (first writer wins).
@@ -119,6 +121,34 @@ enum DeviceError : int32_t {
 void set_last_error(const std::string& msg);
 int32_t* device_error_word();  // device address of the error word for the current device
 cp_status cuda_check(cudaError_t e, const char* what);
+
+// Validates the sizes, dtype and mask of one (query block, key block) pair: the
+// rules every block call shares (Hq % Hkv, D for the dtype, S*H < 2^31, strides,
+// window, positions in int32, n_docs).  On success *m holds the mask to apply
+// (the default causal mask when `mask` is NULL).
+cp_status check_block_args(int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                           const cp_mask* mask, cp_mask* m);
+
+// Gradient destinations of one block backward.  Typed form: dq/dk/dv in the input
+// dtype are overwritten and dq_acc/dk_acc/dv_acc are fp32 scratch.  Accumulating
+// form (typed == false): dq_acc/dk_acc/dv_acc are the caller's fp32 outputs,
+// overwritten (accumulate == 0) or added to (accumulate != 0).
+struct BlockBwdOut {
+  bool typed;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
+  int32_t accumulate;
+};
+// Runs the block backward of a validated call: Delta into `delta` ([Hq, Sq] fp32),
+// the attention backward kernels, and the zero / cast passes the typed form needs.
+cp_status block_bwd_run(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                        const float* lse, int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv, int32_t D,
+                        int32_t dtype, const cp_mask& m, float scale, const BlockBwdOut& o, float* delta,
+                        cudaStream_t st);
 
 // ---------------------------------------------------------------- launchers (one per .cu)
 // movers.cu

@@ -123,29 +123,53 @@ CP_API cp_status cp_attn_block_fwd(const void* q, const void* k, const void* v, 
                             int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask,
                             float scale, void* out, float* lse, void* stream);
 
-/* Backward of cp_attn_block_fwd for the same block pair: the exact gradient of
- * sum(dout * out) given the FINAL out and lse of the rows (for a ring, the
- * merged ones), i.e. P = exp(s - lse), dS = P (dP - rowsum(dout*out)).
- *   dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype` (overwritten; dk/dv are summed
- *   over the Hq/Hkv query heads of each key/value head).  For bf16 with D = 128
- *   the tensor-core kernels write them directly; gradients that share storage
- *   with an input are still correct (then fp32 accumulators in the workspace
- *   are cast after the kernels, as on the FFMA path).
- *   workspace: >= cp_workspace_size(CP_OP_BLOCK_BWD, ...) bytes (fp32 accumulators). */
+/* Backward of cp_attn_block_fwd for the same block pair, accumulating into fp32
+ * gradients, so that a caller can walk the ring of "Ring Attention: passing
+ * the KV once around a ring" one (rank, source) block pair at a time and sum
+ * the pairs' contributions.  The pages give no backward: this is the exact
+ * gradient of sum(dout * out) of the section "Which operations partition
+ * directly"'s attention, given the FINAL out and lse of the query rows (for a
+ * ring, the merged ones, not this pair's partial ones), i.e.
+ * P = exp(scale*s - lse), dS = P (dP - rowsum(dout*out)),
+ * dq = scale * dS k, dk = scale * dS^T q, dv = P^T dout.
+ *   q, out, dout [Sq,Hq,D] and k, v [Sk,Hkv,D] in `dtype`; lse [Hq,Sq] fp32.
+ *   dq_acc [Sq,Hq,D], dk_acc and dv_acc [Sk,Hkv,D]: fp32 device buffers owned
+ *   by the caller.  accumulate = 0 overwrites them with this pair's gradients;
+ *   accumulate = 1 adds this pair's gradients to what they hold.  dk/dv of a
+ *   key/value head are summed over its Hq/Hkv query heads.  They may overlap
+ *   neither an input, the workspace, nor each other (CP_ERR_INVALID_ARG).
+ *   workspace: >= 4*Hq*Sq bytes (Delta = rowsum(dout*out)); the size
+ *   cp_workspace_size(CP_OP_BLOCK_BWD, ...) reports covers it.  Calls on one
+ *   stream that add into the same buffers are ordered by the stream.
+ *   mask, scale and the supported sizes as cp_attn_block_fwd; accumulate other
+ *   than 0 or 1: CP_ERR_INVALID_ARG.  Asynchronous on `stream`. */
 CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, const void* out,
                             const void* dout, const float* lse, int64_t Sq, int64_t Sk, int32_t Hq,
                             int32_t Hkv, int32_t D, int32_t dtype, const cp_mask* mask, float scale,
-                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-                            void* stream);
+                            float* dq_acc, float* dk_acc, float* dv_acc, int32_t accumulate,
+                            void* workspace, size_t ws_bytes, void* stream);
 
-/* cp_attn_block_bwd without a workspace and without any allocation (the pages
- * have no counterpart: this is a library facility).  For callers that may not
- * allocate device memory and have no workspace to hand over: code running
- * behind a plugin or custom-operator interface that passes only input and
- * output buffers, runtimes that plan all device memory ahead of time and
- * forbid allocation afterwards, or processes whose allocator belongs to
+/* The same backward with gradients in the input dtype, overwritten (no
+ * accumulation): dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype`.  For bf16 with
+ * D = 128 the tensor-core kernels write them directly; gradients that share
+ * storage with an input are still correct (then fp32 accumulators in the
+ * workspace are cast after the kernels, as on the FFMA path).
+ *   workspace: >= cp_workspace_size(CP_OP_BLOCK_BWD, ...) bytes (Delta and fp32
+ *   accumulators).  Other arguments as cp_attn_block_bwd. */
+CP_API cp_status cp_attn_block_bwd_typed(const void* q, const void* k, const void* v, const void* out,
+                                         const void* dout, const float* lse, int64_t Sq, int64_t Sk,
+                                         int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                                         const cp_mask* mask, float scale, void* dq, void* dk, void* dv,
+                                         void* workspace, size_t ws_bytes, void* stream);
+
+/* cp_attn_block_bwd_typed without a workspace, allocating no device memory
+ * (the pages have no counterpart: this is a library facility).  For callers
+ * that may not allocate device memory and have no workspace to hand over:
+ * code running behind a plugin or custom-operator interface that passes only
+ * input and output buffers, runtimes that plan all device memory ahead of time
+ * and forbid allocation afterwards, or processes whose allocator belongs to
  * another runtime.  Arguments, layouts and results are those of
- * cp_attn_block_bwd minus the workspace.
+ * cp_attn_block_bwd_typed minus the workspace.
  *   Scratch: a 32 MiB array built into the library (every GPU that loads the
  *   library keeps it until the process exits).  Sizes whose scratch
  *   (4*Hq*Sq + 4*D*(Hq*Sq + 2*Hkv*Sk) bytes, each part rounded up to 256) does
@@ -154,7 +178,8 @@ CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, 
  *   device current); make that first call before any stream capture.
  *   All calls share the array and it keeps the last call's contents (each call
  *   clears what must start at zero): calls that overlap on the GPU race, so
- *   serialise them (one stream per device). */
+ *   serialise them (one stream per device).  Host-side bookkeeping (argument
+ *   checks, the launch schedule) may use the host heap. */
 CP_API cp_status cp_attn_block_bwd_noalloc(const void* q, const void* k, const void* v,
                                            const void* out, const void* dout, const float* lse,
                                            int64_t Sq, int64_t Sk, int32_t Hq, int32_t Hkv,
@@ -322,8 +347,9 @@ CP_API cp_status cp_ulysses_attention_bwd(const void* q, const void* k, const vo
 
 /* Workspace bytes needed by `op` (a cp_op) for these sizes; `mode` is the
  * cp_ring_mode for CP_OP_RING_FWD and ignored otherwise.  For CP_OP_BLOCK_BWD
- * pass S = max(Sq, Sk) (P is ignored).  Returns CP_OK and
- * writes *bytes, or an error for invalid sizes. */
+ * pass S = max(Sq, Sk) (P is ignored): the size serves both cp_attn_block_bwd
+ * and cp_attn_block_bwd_typed.  Returns CP_OK and writes *bytes, or an error
+ * for invalid sizes. */
 CP_API cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hkv, int32_t D,
                             int32_t dtype, int32_t P, int32_t mode, size_t* bytes);
 

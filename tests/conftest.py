@@ -10,3 +10,25 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Worst margin per test: max error against its bound, for every GPU parity check."""
+    try:
+        from gpu_common import MARGINS
+    except Exception:
+        return
+    if not MARGINS:
+        return
+    worst = {}
+    for test, what, err, bound in MARGINS:
+        r = err / bound if bound > 0 else 0.0
+        if test not in worst or r > worst[test][0]:
+            worst[test] = (r, what, err, bound)
+    tr = terminalreporter
+    tr.write_sep("-", f"parity margins: {len(MARGINS)} checks, worst error / bound per test")
+    rows = sorted(worst.items(), key=lambda x: -x[1][0])
+    for test, (r, what, err, bound) in rows[:30]:
+        tr.write_line(f"{r:6.3f}  {err:.3g} <= {bound:.3g}  {test} [{what}]")
+    if len(rows) > 30:
+        tr.write_line(f"... {len(rows) - 30} more tests, each at most {rows[30][1][0]:.3f} of its bound")

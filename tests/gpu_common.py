@@ -1,6 +1,7 @@
 """Shared helpers for the GPU parity tests (inputs come from synth, expected
 values only from the oracle)."""
 import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -36,12 +37,51 @@ def max_err(gpu, ref):
     return float(np.nan_to_num(d, nan=np.inf).max()) if d.size else 0.0
 
 
+# (test, quantity, max error, bound) of every checked result, printed in the
+# terminal summary so the margins to the bounds are visible in a quiet run.
+MARGINS = []
+
+
+def _record(what, err, bound):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0].split("::")[-1]
+    MARGINS.append((test, what, float(err), float(bound)))
+
+
 def assert_close(gpu_out, gpu_lse, ref_out, ref_lse, dtype, what=""):
     eo = max_err(gpu_out, ref_out)
     el = max_err(gpu_lse, ref_lse)
+    _record(f"{what} out", eo, TOL_OUT[dtype])
+    _record(f"{what} lse", el, TOL_LSE)
     assert eo <= TOL_OUT[dtype], f"{what}: out max err {eo}"
     assert el <= TOL_LSE, f"{what}: lse max err {el}"
     return eo, el
+
+
+def check_grad(name, got, ref, tol):
+    """Gradient bound (reading R11): max |err| <= tol * max(1, max |ref|)."""
+    e = max_err(got, ref)
+    bound = tol * max(1.0, float(np.abs(np.asarray(ref, dtype=np.float64)).max()) if np.size(ref) else 1.0)
+    _record(name, e, bound)
+    assert e <= bound, f"{name}: max err {e} > bound {bound}"
+    return e
+
+
+def oracle_bwd_by_kv_head(q, k, v, do, workers=4, **kw):
+    """oracle.attention_bwd applied to each key/value head with its G query heads
+    (one call per head on a thread pool) and reassembled.  The definition treats
+    heads independently, so this is the same gradient as one call on all heads."""
+    import oracle
+
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = Hq // Hkv
+
+    def one(hk):
+        hs = slice(hk * G, (hk + 1) * G)
+        return oracle.attention_bwd(q[:, hs], k[:, hk:hk + 1], v[:, hk:hk + 1], do[:, hs], **kw)
+
+    with ThreadPoolExecutor(max(1, min(workers, Hkv))) as ex:
+        parts = list(ex.map(one, range(Hkv)))
+    return tuple(np.concatenate([p[i] for p in parts], axis=1) for i in range(3))
 
 
 def check_ok():

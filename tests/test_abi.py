@@ -189,3 +189,44 @@ def test_merge_and_workspace_refusals(lib):
     assert lib.cp_workspace_size(0, 8192, 32, 32, 128, 1, 8, 1, ctypes.byref(out)) == 0
     assert out.value > fused  # stepwise keeps fp32 partials
     assert lib.cp_debug_bounded_wait(0, None) == -1
+
+
+def _bwd(lib, **kw):
+    args = dict(q=P16, k=P16, v=P16, out=P16, dout=P16, lse=P16, Sq=128, Sk=128, Hq=8, Hkv=8, D=128,
+                dtype=1, mask=None, scale=0.0, dq=ctypes.c_void_p(1 << 30), dk=ctypes.c_void_p(1 << 31),
+                dv=ctypes.c_void_p(1 << 32), acc=0, ws=ctypes.c_void_p(1 << 33), ws_bytes=1 << 20,
+                stream=None)
+    args.update(kw)
+    return lib.cp_attn_block_bwd(*args.values())
+
+
+def test_accumulating_block_bwd_refusals(lib):
+    # the accumulating form (fp32 gradient buffers + accumulate flag): refused before any launch
+    assert _bwd(lib, acc=2) == -1                         # accumulate is 0 or 1
+    assert _bwd(lib, dq=P16) == -1                        # dq_acc overlaps q
+    assert "overlap" in cpa.cp_last_error()
+    assert _bwd(lib, dk=ctypes.c_void_p(1 << 30)) == -1   # dk_acc overlaps dq_acc
+    assert _bwd(lib, ws_bytes=100) == -6                  # Delta needs 4*Hq*Sq bytes
+    assert _bwd(lib, ws=ctypes.c_void_p(0)) == -6
+    assert _bwd(lib, dv=ctypes.c_void_p((1 << 32) + 4)) == -4  # misaligned
+    assert _bwd(lib, D=96) == -3
+    assert _bwd(lib, Sq=0, Sk=0) == 0                     # empty is a no-op
+
+
+def test_noalloc_refuses_absurd_sizes_without_a_device(lib):
+    # the shared validation runs first: sizes whose scratch arithmetic could wrap are
+    # refused by the S*H < 2^31 and int32-position rules, never by a wrapped size
+    f = lib.cp_attn_block_bwd_noalloc
+    base = [P16, P16, P16, P16, P16, P16, 1 << 40, 128, 8, 8, 128, 1, None, 0.0, P16, P16, P16, None]
+    assert f(*base) == -5 and "2^31" in cpa.cp_last_error()
+    m = cpa.cp_mask()
+    m.causal, m.q_stride, m.k_stride, m.q_offset = 1, 1, 1, -(1 << 63)
+    a = list(base)
+    a[6], a[12] = 128, ctypes.byref(m)
+    assert f(*a) == -5 and "int32" in cpa.cp_last_error()
+    m.q_offset, m.q_stride = 0, 1 << 62                   # stride * (Sq - 1) would overflow int64
+    assert f(*a) == -5
+    a = list(base)
+    a[6], a[7] = 8192, 8192                               # valid, but beyond the built-in scratch
+    a[8], a[9] = 32, 8
+    assert f(*a) == -5 and "built-in scratch" in cpa.cp_last_error()

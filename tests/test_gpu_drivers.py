@@ -12,7 +12,8 @@ import torch
 
 import context_causal_attention_tcgen05_gb300 as cpa
 import oracle
-from gpu_common import TOL_OUT, assert_close, check_ok, f64, max_err, need_gpu, sample_rows
+from gpu_common import (TOL_OUT, assert_close, check_grad, check_ok, f64, max_err, need_gpu,
+                        oracle_bwd_by_kv_head, sample_rows)
 from synth import cu_seqlens_from_lengths, doc_lengths, make_inputs, make_qkv
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +57,7 @@ def test_tiny_exact_ring_bwd(layout):
     dq, dk, dv = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), 4, layout)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        assert max_err(got, ref) <= 1e-4 * max(1.0, float(np.abs(ref).max())), name
+        check_grad(name, got, ref, 1e-4)
     check_ok()
 
 
@@ -114,7 +115,7 @@ def test_tiny_exact_ulysses_bwd():
     dq, dk, dv = cpa.cp_ulysses_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), 4)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        assert max_err(got, ref) <= TOL_OUT[torch.float32] * max(1.0, float(np.abs(ref).max())), name
+        check_grad(name, got, ref, TOL_OUT[torch.float32])
     check_ok()
 
 
@@ -132,7 +133,7 @@ def test_ulysses_bwd_bf16_medium(Hq, Hkv, P, D, docs):
                                               cu_seqlens=cu_d)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+        check_grad(name, got, ref, 2e-2)
     check_ok()
 
 
@@ -174,7 +175,7 @@ def test_ulysses_window_fwd_bwd(Hq, Hkv, P, W, docs):
                                               cu_seqlens=cu_d, window=W)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu, window=W)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+        check_grad(name, got, ref, 2e-2)
     check_ok()
 
 
@@ -190,7 +191,7 @@ def test_ring_bwd_bf16_medium(layout, docs):
                                            cu_seqlens=cu_d)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, cu_seqlens=cu)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        assert max_err(got, ref) <= 2e-2 * max(1.0, float(np.abs(ref).max())), name
+        check_grad(name, got, ref, 2e-2)
     check_ok()
 
 
@@ -274,15 +275,13 @@ def test_full_gqa_ring_fwd_bwd_s65536_p4_zigzag():
     allpos = np.arange(S)
     # dQ on sampled rows
     rq, _, _ = oracle.attention_bwd(q[rows], k, v, do[rows], True, pos_q=rows, pos_k=allpos)
-    e = max_err(dq[torch.from_numpy(rows).cuda()], rq)
-    assert e <= 2e-2 * max(1.0, float(np.abs(rq).max())), f"dq {e}"
+    check_grad("dq sampled rows", dq[torch.from_numpy(rows).cuda()], rq, 2e-2)
     # dK / dV of the last T key rows
     T = 64
     tail = np.arange(S - T, S)
     _, rk, rv = oracle.attention_bwd(q[S - T:], k, v, do[S - T:], True, pos_q=tail, pos_k=allpos)
     for name, got, ref in (("dk", dk[S - T:], rk[S - T:]), ("dv", dv[S - T:], rv[S - T:])):
-        e = max_err(got, ref)
-        assert e <= 2e-2 * max(1.0, float(np.abs(ref).max())), f"{name} {e}"
+        check_grad(f"{name} last {T} key rows", got, ref, 2e-2)
     # identities over all rows (fp64 sums of the GPU result vs of the inputs)
     dv_sum = dv.double().sum(0).cpu().numpy()             # [Hkv, D]
     do_sum = do.double().sum(0).reshape(Hkv, G, D).sum(1).numpy()
@@ -307,17 +306,122 @@ def test_full_ulysses_bwd_s32768_h32_p16():
     allpos = np.arange(S)
     rows = sample_rows(S, P, "contiguous", 16)
     rq, _, _ = oracle.attention_bwd(q[rows], k, v, do[rows], True, pos_q=rows, pos_k=allpos)
-    e = max_err(dq[torch.from_numpy(rows).cuda()], rq)
-    assert e <= 2e-2 * max(1.0, float(np.abs(rq).max())), f"dq {e}"
+    check_grad("dq sampled rows", dq[torch.from_numpy(rows).cuda()], rq, 2e-2)
     T = 48
     tail = np.arange(S - T, S)
     _, rk, rv = oracle.attention_bwd(q[S - T:], k, v, do[S - T:], True, pos_q=tail, pos_k=allpos)
     for name, got, ref in (("dk", dk[S - T:], rk[S - T:]), ("dv", dv[S - T:], rv[S - T:])):
-        e = max_err(got, ref)
-        assert e <= 2e-2 * max(1.0, float(np.abs(ref).max())), f"{name} {e}"
+        check_grad(f"{name} last {T} key rows", got, ref, 2e-2)
     dv_sum = dv.double().sum(0).cpu().numpy()
     do_sum = do.double().sum(0).numpy()
     assert np.abs(dv_sum - do_sum).max() <= 1e-2 * max(1.0, np.abs(do_sum).max()), "sum dV"
     dk_sum = dk.double().sum(0).cpu().numpy()
     dk_scale = dk.double().abs().sum(0).cpu().numpy().max()
     assert np.abs(dk_sum).max() <= 1e-3 * dk_scale, "sum dK"
+
+
+# ---------------------------------------------------------------- every gradient element at the bench's tile counts
+
+@pytest.mark.parametrize("docs", [False, True], ids=["causal", "packed_docs"])
+def test_ring_bwd_gqa_s8192_p4_zigzag_every_element(docs):
+    """The GQA ring backward (Hq=32, Hkv=8, D=128, P=4 zigzag) at S=8192, where the
+    key-stationary kernel runs 512 CTAs (several waves, heaviest first) and walks
+    runs of up to 64 query tiles through the mask-free path: every element of dQ,
+    dK and dV against the oracle's gradient of unpartitioned attention."""
+    S, Hq, Hkv, D, P = 8192, 32, 8, 128, 4
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=9, with_dout=True)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 256, 2048, seed=7)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, l = cpa.cp_ring_attention(qd, kd, vd, P, "zigzag", "fused", cu_seqlens=cu_d)
+    dq, dk, dv = cpa.cp_ring_attention_bwd(qd, kd, vd, o, l, dod, P, "zigzag", cu_seqlens=cu_d)
+    check_ok()
+    rq, rk, rv = oracle_bwd_by_kv_head(q, k, v, do, causal=True, cu_seqlens=cu)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        check_grad(name, got, ref, 2e-2)
+
+
+def test_ulysses_bwd_s8192_hq32_hkv8_p16_every_element():
+    """The Ulysses backward with 16 virtual ranks (2 query heads each; each of the 8
+    key/value heads replicated twice) at S=8192: every element of dQ, dK and dV."""
+    S, Hq, Hkv, D, P = 8192, 32, 8, 128, 16
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=10, with_dout=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, l = cpa.cp_ulysses_attention(qd, kd, vd, P)
+    dq, dk, dv = cpa.cp_ulysses_attention_bwd(qd, kd, vd, o, l, dod, P)
+    check_ok()
+    rq, rk, rv = oracle_bwd_by_kv_head(q, k, v, do, causal=True)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        check_grad(name, got, ref, 2e-2)
+
+
+# ---------------------------------------------------------------- the ring backward one block pair at a time
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float32, 64), (torch.bfloat16, 64)],
+                         ids=["bf16_d128", "f32_d64", "bf16_d64"])
+def test_ring_bwd_composed_from_accumulating_block_calls(dtype, D):
+    """The handbook's ring ("Ring Attention: passing the KV once around a ring"),
+    contiguous layout, P=4: rank r's queries meet the key/value block of every
+    source src <= r.  Each pair is one cp_attn_block_bwd call with the FINAL
+    (unpartitioned) out and lse of rank r's rows, adding into fp32 dQ / dK / dV
+    (the first contribution to a block overwrites garbage, the rest accumulate).
+    The sums equal the gradient of unpartitioned attention."""
+    S, Hq, Hkv, P = 1024, 4, 2, 4
+    C = S // P
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, dtype, seed=23, with_dout=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, l = cpa.cp_attn_block_fwd(qd, kd, vd, True)  # the final out and lse of every row
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dq = torch.full((S, Hq, D), float("nan"), **f32)  # garbage the first call must overwrite
+    dk = torch.full((S, Hkv, D), float("nan"), **f32)
+    dv = torch.full((S, Hkv, D), float("nan"), **f32)
+    seen_q, seen_k = set(), set()
+    for r in range(P):
+        rq = slice(r * C, (r + 1) * C)
+        lse_r = l[:, rq].contiguous()
+        for src in range(r, -1, -1):  # ring order: own block first, then r-1, ...
+            rk = slice(src * C, (src + 1) * C)
+            # one call per pair; a block written for the first time is overwritten
+            first_q, first_k = r not in seen_q, src not in seen_k
+            if first_q != first_k:
+                # the call's one accumulate flag covers all three outputs: give the block
+                # seen for the first time a zeroed start instead
+                if first_q:
+                    dq[rq].zero_()
+                else:
+                    dk[rk].zero_()
+                    dv[rk].zero_()
+            acc = not (first_q and first_k)
+            cpa.cp_attn_block_bwd(qd[rq], kd[rk], vd[rk], o[rq], dod[rq], lse_r, True, r * C, src * C,
+                                  dq_acc=dq[rq], dk_acc=dk[rk], dv_acc=dv[rk], accumulate=acc)
+            seen_q.add(r)
+            seen_k.add(src)
+    check_ok()
+    ref = oracle.attention_bwd(q, k, v, do, True)
+    tol = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        check_grad(name, got, want, tol)
+
+
+def test_block_bwd_accumulate_flag_adds_and_overwrites():
+    """accumulate = 0 replaces what the fp32 buffers hold; accumulate = 1 adds to it."""
+    S, Hq, Hkv, D = 300, 4, 2, 128
+    q, k, v, do = (t.cuda() for t in make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=24, with_dout=True))
+    o, l = cpa.cp_attn_block_fwd(q, k, v, True)
+    base = cpa.cp_attn_block_bwd(q, k, v, o, do, l, True)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    start = [torch.randn(t.shape, **f32) for t in base]
+    bufs = [t.clone() for t in start]
+    cpa.cp_attn_block_bwd(q, k, v, o, do, l, True, dq_acc=bufs[0], dk_acc=bufs[1], dv_acc=bufs[2],
+                          accumulate=True)
+    for b, s0, g in zip(bufs, start, base):
+        assert torch.allclose(b, s0 + g, rtol=0, atol=1e-5)
+    cpa.cp_attn_block_bwd(q, k, v, o, do, l, True, dq_acc=bufs[0], dk_acc=bufs[1], dv_acc=bufs[2],
+                          accumulate=False)
+    for b, g in zip(bufs, base):
+        assert torch.equal(b, g)
+    # the typed form is the accumulating form's result rounded once
+    typed = cpa.cp_attn_block_bwd_typed(q, k, v, o, do, l, True)
+    for t, g in zip(typed, base):
+        assert torch.equal(t, g.to(torch.bfloat16))
+    check_ok()

@@ -10,7 +10,7 @@ import torch
 
 import context_causal_attention_tcgen05_gb300 as cpa
 import oracle
-from gpu_common import TOL_LSE, TOL_OUT, assert_close, check_ok, f64, max_err, need_gpu
+from gpu_common import TOL_LSE, TOL_OUT, assert_close, check_grad, check_ok, f64, max_err, need_gpu
 from synth import cu_seqlens_from_lengths, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -169,13 +169,12 @@ def test_block_bwd_window(dtype, case):
     cu = None if docs is None else cu_seqlens_from_lengths(docs)
     cu_d = None if cu is None else torch.from_numpy(cu).cuda()
     o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), True, qo, ko, 1, 1, cu_d, window=W)
-    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, True, qo, ko, 1, 1, cu_d,
+    dq, dk, dv = cpa.cp_attn_block_bwd_typed(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, True, qo, ko, 1, 1, cu_d,
                                        window=W)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, True, qo, ko, cu_seqlens=cu, window=W)
     tol = TOL_OUT[dtype] if dtype == torch.float32 else 2e-2
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        e = max_err(got, ref)
-        assert e <= tol * max(1.0, float(np.abs(ref).max())), f"{name} {case}: {e}"
+        check_grad(f"{name} {case}", got, ref, tol)
     check_ok()
 
 
@@ -209,13 +208,11 @@ def test_block_bwd(dtype, case):
     cu_d = None if cu is None else torch.from_numpy(cu).cuda()
     # forward on the GPU gives the (out, lse) the backward consumes, as in training
     o, l = cpa.cp_attn_block_fwd(q.cuda(), k.cuda(), v.cuda(), causal, qo, ko, 1, 1, cu_d)
-    dq, dk, dv = cpa.cp_attn_block_bwd(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, causal, qo, ko, 1, 1, cu_d)
+    dq, dk, dv = cpa.cp_attn_block_bwd_typed(q.cuda(), k.cuda(), v.cuda(), o, do.cuda(), l, causal, qo, ko, 1, 1, cu_d)
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal, qo, ko, cu_seqlens=cu)
     tol = TOL_OUT[dtype] if dtype == torch.float32 else 2e-2
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        e = max_err(got, ref)
-        scale = max(1.0, float(np.abs(ref).max()))
-        assert e <= tol * scale, f"{name} {case}: {e}"
+        check_grad(f"{name} {case}", got, ref, tol)
     check_ok()
 
 
@@ -281,14 +278,14 @@ def test_block_bwd_gradient_aliasing_an_input():
     q, k, v, do = (torch.randn(S, H, D, generator=g).to(torch.bfloat16).cuda()
                    for S, H in ((Sq, Hq), (Sk, Hkv), (Sk, Hkv), (Sq, Hq)))
     o, l = cpa.cp_attn_block_fwd(q, k, v, True)
-    dq_ref, dk_ref, dv_ref = cpa.cp_attn_block_bwd(q, k, v, o, do, l, True)
+    dq_ref, dk_ref, dv_ref = cpa.cp_attn_block_bwd_typed(q, k, v, o, do, l, True)
     buf = do.clone()  # dout and dq share this storage
     dk, dv = torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(cpa.cp_workspace_size("block_bwd", Sq, Hq, Hkv, D, q.dtype, 1), dtype=torch.uint8,
                      device="cuda")
     m = cpa._mask(True, 0, 0, 1, 1, None, 0)
     lib = cpa.load_library()
-    st = lib.cp_attn_block_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), buf.data_ptr(),
+    st = lib.cp_attn_block_bwd_typed(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), buf.data_ptr(),
                                l.data_ptr(), Sq, Sk, Hq, Hkv, D, cpa.CP_BF16, ctypes.byref(m), 0.0,
                                buf.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
                                torch.cuda.current_stream().cuda_stream)
