@@ -42,6 +42,17 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
+def _r(x, sig: int = 4):
+    """Floats rounded to `sig` significant digits, recursively (keeps the line short)."""
+    if isinstance(x, float):
+        return float(f"{x:.{sig}g}") if math.isfinite(x) else x
+    if isinstance(x, dict):
+        return {k: _r(v, sig) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [_r(v, sig) for v in x]
+    return x
+
+
 def causal_flop(S: int, H: int, D: int) -> float:
     """4*D FLOP per visible (query, key) pair per head (QK^T and PV)."""
     return 4.0 * D * H * (S * (S + 1) // 2)
@@ -578,22 +589,11 @@ def bench_ours(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "attn_fwd_tc (ring, fused)", "peak_source": peaks["source"] + " burst bf16"},
-            "fwd_bwd": None if fb is None else dict(fb, frac_of_peak=fb["fwd_bwd_tflops"] / peak),
-            "hbm_kernels": {k: dict(v, frac_of_hbm=v["gbs"] / peaks["hbm_gbs"]) for k, v in hbm.items()},
-            "ulysses_fwd": None if uly is None else dict(
-                uly, frac_of_peak=uly["attention_tflops"] / peak,
-                permute_frac_of_hbm=uly["permute_gbs"] / peaks["hbm_gbs"],
-                fwd_bwd_frac_of_peak=uly["fwd_bwd_tflops"] / peak),
-            "varlen_fwd": None if vlen is None else dict(
-                vlen, frac_of_peak={k: vlen[k]["tflops"] / peak for k in ("striped", "zigzag")}),
-            "parts": {"attention_ms": attn_mean, "attention_tflops": achieved,
-                      "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
-                      "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]},
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * tensor_bytes,
-                    "d2h_bytes_per_step": tensor_bytes + S * H * 4, "ms_per_step": e2e_mean,
-                    "pipeline": "2 buffer sets; copy-in, compute, copy-out on 3 streams",
-                    "serial_ms_per_step": e2e_serial,
-                    "serial_value": flop / (e2e_serial * 1e-3) / 1e12},
+            "e2e": _r({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 3 * tensor_bytes,
+                       "d2h_bytes_per_step": tensor_bytes + S * H * 4, "ms_per_step": e2e_mean,
+                       "pipeline": "2 buffer sets; copy-in, compute, copy-out on 3 streams",
+                       "serial_ms_per_step": e2e_serial,
+                       "serial_value": flop / (e2e_serial * 1e-3) / 1e12}),
             "clocks": clocks,
         }
         if cpu_tf is not None:
@@ -601,9 +601,87 @@ def bench_ours(args):
                                     "sample": f"{cpu_rows} random query rows x {H} heads, full causal key "
                                               f"range ({cpu_s:.1f} s of float64 CPU work)",
                                     "host": host_info()}
+        # the other workloads' parts, the fwd+bwd of the largest one last
+        line["parts"] = _r({"attention_ms": attn_mean, "attention_tflops": achieved,
+                            "permute_ms": statistics.mean(perm_ms), "permute_gbs": perm_gbs,
+                            "permute_frac_of_hbm": perm_gbs / peaks["hbm_gbs"]})
+        line["hbm_kernels"] = _r({k: {"ms": v["ms"], "gbs": v["gbs"], "frac_of_hbm": v["gbs"] / peaks["hbm_gbs"]}
+                                  for k, v in hbm.items()})
+        if uly is not None:
+            line["ulysses_fwd"] = _r(dict(uly, frac_of_peak=uly["attention_tflops"] / peak,
+                                          permute_frac_of_hbm=uly["permute_gbs"] / peaks["hbm_gbs"],
+                                          fwd_bwd_frac_of_peak=uly["fwd_bwd_tflops"] / peak))
+        if vlen is not None:
+            for lay in ("striped", "zigzag"):
+                vlen[lay].pop("rank_visible_pairs", None)
+            line["varlen_fwd"] = _r(dict(vlen, frac_of_peak={k: vlen[k]["tflops"] / peak
+                                                             for k in ("striped", "zigzag")}))
+        if fb is not None:
+            line["fwd_bwd"] = _r(dict(fb, fwd_frac_of_peak=fb["fwd_tflops"] / peak,
+                                      bwd_frac_of_peak=fb["bwd_tflops"] / peak,
+                                      frac_of_peak=fb["fwd_bwd_tflops"] / peak))
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def profile_case(args) -> int:
+    """Runs one hot-path case a few times on cuda:0, for profiler captures (ncu):
+    ring_fwd (reordered inputs, fused ring: one attention launch per rep), ring_bwd
+    (ring backward), permute (zigzag reorder of q), reorder_qkv (q, k, v in one
+    launch), ulysses (seq2head of q), merge (in-place fp32 or bf16 LSE merge of two
+    [S, Hq, D] partial outputs).  Inputs are N(0,1) bf16 from the seeded
+    generators.  Returns non-zero if the library reports an error."""
+    import context_causal_attention_tcgen05_gb300 as cpa
+    from synth import make_inputs
+
+    a = args
+    torch.cuda.set_device(0)
+    cpa.load_library()
+    q, k, v, do = (t.cuda() for t in make_inputs(a.S, a.Hq, a.Hkv, a.D, torch.bfloat16, 0, True))
+    cu_d = None
+    if a.docs:
+        from synth import cu_seqlens_from_lengths, doc_lengths
+        cu_d = torch.from_numpy(cu_seqlens_from_lengths(doc_lengths(a.S, 512, 16384, seed=0))).cuda()
+    if a.profile_case == "ring_fwd":
+        reo = {"zigzag": cpa.cp_zigzag_reorder, "striped": cpa.cp_striped_reorder}.get(a.layout)
+        qr, kr, vr = (reo(x, a.P) if reo else x for x in (q, k, v))
+        for _ in range(a.reps):
+            cpa.cp_ring_attention_reordered(qr, kr, vr, a.P, a.layout, "fused", cu_seqlens=cu_d)
+    elif a.profile_case == "ring_bwd":
+        o, l = cpa.cp_ring_attention(q, k, v, a.P, a.layout, "fused", cu_seqlens=cu_d)
+        ws = torch.empty(cpa.cp_workspace_size("ring_bwd", a.S, a.Hq, a.Hkv, a.D, q.dtype, a.P),
+                         dtype=torch.uint8, device=q.device)
+        for _ in range(a.reps):
+            cpa.cp_ring_attention_bwd(q, k, v, o, l, do, a.P, a.layout, cu_seqlens=cu_d, workspace=ws)
+    elif a.profile_case == "merge":
+        g = torch.Generator(device="cuda").manual_seed(1)
+        dt = torch.bfloat16 if a.merge_dtype == "bf16" else torch.float32
+        o1 = torch.randn(a.S, a.Hq, a.D, device="cuda", generator=g).to(dt)
+        o2 = torch.randn(a.S, a.Hq, a.D, device="cuda", generator=g).to(dt)
+        l1 = torch.randn(a.Hq, a.S, device="cuda", generator=g)
+        l2 = torch.randn(a.Hq, a.S, device="cuda", generator=g)
+        for _ in range(a.reps):
+            cpa.cp_lse_merge(o1, l1, o2, l2, out=o1, lse=l1)
+    elif a.profile_case == "reorder_qkv":
+        ys = [torch.empty_like(x) for x in (q, k, v)]
+        for _ in range(a.reps):
+            cpa.cp_ring_reorder_qkv(q, k, v, a.P, a.layout, q_re=ys[0], k_re=ys[1], v_re=ys[2])
+    elif a.profile_case == "permute":
+        y = torch.empty_like(q)
+        for _ in range(a.reps):
+            cpa.cp_zigzag_reorder(q, a.P, y=y)
+    else:  # ulysses
+        y = torch.empty(a.P, a.S, a.Hq // a.P, a.D, dtype=q.dtype, device=q.device)
+        for _ in range(a.reps):
+            cpa.cp_ulysses_seq2head(q, a.P, y=y)
+    torch.cuda.synchronize()
+    st = cpa.cp_check_device_status()
+    if st != 0:
+        print("device status", st, cpa.cp_last_error(), file=sys.stderr)
+        return 1
+    print("ok")
+    return 0
 
 
 def main():
@@ -614,7 +692,21 @@ def main():
     ap.add_argument("--fwd-bwd-steps", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # one profiler case instead of the benchmark (see profile_case)
+    ap.add_argument("--profile-case", choices=["ring_fwd", "ring_bwd", "permute", "reorder_qkv", "ulysses",
+                                               "merge"])
+    ap.add_argument("--S", type=int, default=8192)
+    ap.add_argument("--Hq", type=int, default=32)
+    ap.add_argument("--Hkv", type=int, default=32)
+    ap.add_argument("--D", type=int, default=128)
+    ap.add_argument("--P", type=int, default=8)
+    ap.add_argument("--layout", default="zigzag")
+    ap.add_argument("--docs", action="store_true", help="pack documents (lengths U[512, 16384], seed 0)")
+    ap.add_argument("--merge-dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        sys.exit(profile_case(args))
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -28,7 +28,10 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     tr = terminalreporter
     tr.write_sep("-", f"parity margins: {len(MARGINS)} checks, worst error / bound per test")
     rows = sorted(worst.items(), key=lambda x: -x[1][0])
-    for test, (r, what, err, bound) in rows[:30]:
+    # the worst 20, then every full-size workload's check (the sizes the bench times)
+    shown = rows[:20] + [r for r in rows[20:] if "full" in r[0] or "every_element" in r[0]]
+    for test, (r, what, err, bound) in shown:
         tr.write_line(f"{r:6.3f}  {err:.3g} <= {bound:.3g}  {test} [{what}]")
-    if len(rows) > 30:
-        tr.write_line(f"... {len(rows) - 30} more tests, each at most {rows[30][1][0]:.3f} of its bound")
+    if len(rows) > len(shown):
+        rest = [r for r in rows if r not in shown]
+        tr.write_line(f"... {len(rest)} more tests, each at most {rest[0][1][0]:.3f} of its bound")

@@ -40,7 +40,8 @@ def _bound(ref, tol):
 @pytest.mark.parametrize("docs_window", [False, True], ids=["causal", "docs_window"])
 def test_noalloc_matches_workspace_entry_point_and_oracle_twice(dtype, D, tol, docs_window):
     S, Hq, Hkv = 384, 8, 2
-    cu = cu_seqlens_from_lengths([100, 1, 150, 133]) if docs_window else None
+    # documents cover every position the call sees: keys 0..383, queries 64..447
+    cu = cu_seqlens_from_lengths([100, 1, 150, 133, 64]) if docs_window else None
     W = 90 if docs_window else 0
     cu_d = None if cu is None else torch.from_numpy(cu).cuda()
     for seed in (11, 12):  # two calls in a row, different inputs
