@@ -16,7 +16,10 @@ import re
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcp_attn.so")
+# CP_ATTN_LIBRARY may name another build of the library (the index-checking debug
+# build, libcp_attn_debug.so); it must exist: there is no fallback either way.
+LIB_PATH = os.environ.get("CP_ATTN_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                            "libcp_attn.so")
 
 __all__ = [
     "CpAttnError", "load_library", "library_path", "header_functions",

@@ -294,14 +294,22 @@ int32_t resolve_layout(int32_t reorder, const int32_t* cu) {
   return reorder;
 }
 
-cp_status launch_fwd(const AttnArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
+cp_status launch_fwd(const AttnArgs& a0, Schedule& s, int32_t dtype, int64_t q_rows,
                      int64_t k_rows, cudaStream_t st) {
+  // buffer extents for the debug build's index checks: q and o share their rows; the
+  // lse array holds the heads the schedule's groups reach
+  AttnArgs a = a0;
+  a.q_rows = q_rows;
+  a.k_rows = k_rows;
+  int64_t heads = 0;
+  for (int i = 0; i < s.n_groups; ++i) heads = std::max<int64_t>(heads, (int64_t)s.g[i].lse_head0 + a.Hq);
+  a.lse_size = heads * a.lse_ld;
   if (dtype == CP_BF16) return launch_attn_fwd_tc(a, s, q_rows, k_rows, st);
   return launch_attn_fwd_simt(a, s, 0, st);
 }
 
 }  // namespace
-bool cpa::bwd_writes_bf16(int32_t dtype, int32_t D) { return dtype == CP_BF16 && D == 128; }
+bool cpa::bwd_writes_bf16(int32_t dtype, int32_t D) { return dtype == CP_BF16 && (D == 64 || D == 128); }
 
 bool cpa::grads_apart(const void* const* outs, const size_t* out_bytes, int n_out, const void* const* ins,
                       const size_t* in_bytes, int n_in) {
@@ -315,9 +323,13 @@ bool cpa::grads_apart(const void* const* outs, const size_t* out_bytes, int n_ou
 }
 namespace {
 
-cp_status launch_bwd(const BwdArgs& a, Schedule& s, int32_t dtype, int64_t q_rows,
+cp_status launch_bwd(const BwdArgs& a0, Schedule& s, int32_t dtype, int64_t q_rows,
                      int64_t k_rows, cudaStream_t st) {
-  // The tensor-core backward is written for D = 128; other head sizes use the FFMA kernel.
+  BwdArgs a = a0;  // buffer extents for the debug build's index checks
+  a.q_rows = q_rows;
+  a.k_rows = k_rows;
+  a.lse_size = (int64_t)a.Hq * a.lse_ld;
+  // bf16 runs on the tensor-core kernels (D = 64 or 128); fp32 on the exact FFMA kernel.
   if (bwd_writes_bf16(dtype, a.D)) return launch_attn_bwd_tc(a, s, q_rows, k_rows, st);
   return launch_attn_bwd_simt(a, s, dtype == CP_BF16, st);
 }
@@ -657,6 +669,7 @@ const char* cp_status_string(int32_t st) {
     case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
     case CP_ERR_CUDA: return "CP_ERR_CUDA";
     case CP_ERR_DEVICE_TIMEOUT: return "CP_ERR_DEVICE_TIMEOUT";
+    case CP_ERR_DEVICE_INDEX: return "CP_ERR_DEVICE_INDEX";
     default: return "CP_ERR_UNKNOWN";
   }
 }
@@ -1422,6 +1435,10 @@ cp_status cp_check_device_status(void* stream) {
   if (code != 0) {
     int32_t zero = 0;
     (void)cudaMemcpy(ew, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (code == kDevIndex) {
+      set_last_error("a kernel's index check failed and skipped the access (debug build)");
+      return CP_ERR_DEVICE_INDEX;
+    }
     set_last_error("a kernel gave up on a bounded wait (device error code " +
                    std::to_string(code) + ")");
     return CP_ERR_DEVICE_TIMEOUT;

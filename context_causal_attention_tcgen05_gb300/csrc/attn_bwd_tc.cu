@@ -1,4 +1,4 @@
-// tcgen05 block attention backward for bf16 (fp32 accumulation), D = 128.
+// tcgen05 block attention backward for bf16 (fp32 accumulation), D = 64 or 128.
 //
 // The exact derivative of the handbook's attention ("Context parallelism:
 // Ring Attention and Ulysses", section "Which operations partition
@@ -26,16 +26,19 @@
 //   has the next tile's scores queued while the softmax works.  lse and Delta
 //   of each query tile are staged with cp.async alongside the Q/dO tiles.
 //
-// attn_bwd_dq_kernel: one CTA = one 128-row query tile of one query head.  The
-//   softmax warps copy Q and dO into TMEM once (A operands); the CTA walks
-//   every 128-key tile it sees (a query-major schedule, as in the forward):
-//     S = Q K^T (TMEM 0..127), dP = dO V^T (TMEM 128..255)
+// attn_bwd_dq_kernel: one CTA = one 128-row query tile of one query head.  Q and
+//   dO are loaded once into shared memory; the CTA walks every 128-key tile it
+//   sees (a query-major schedule, as in the forward), K in a 3-stage and V in a
+//   2-stage ring:
+//     S = Q K^T (TMEM 0..127), dP = dO V^T (TMEM 128..255 for even tiles,
+//     384..511 for odd ones)
 //     softmax warps (thread = query row, each warpgroup 64 of the key columns):
-//       phase 1 P from S (then S is free for the next tile), phase 2 dS once
-//       dP lands, written over dP
+//       phase 1 P from S (S is released as soon as it is in registers), phase 2
+//       dS once dP lands, written over dP in the same buffer
 //     dQ += dS K (TMEM 256..383)
-//   MMA issue order S_{j+1}, dQ_j, dP_{j+1}.  Q, dO in TMEM 384..447, 448..511.
-//
+//   MMA issue order S_{j+1}, dP_{j+1}, dQ_j: with two dP / dS buffers dP_{j+1}
+//   does not wait for dQ_j, so the softmax's second phase of tile j+1 finds its
+//   dP ready.
 // This recomputes S and dP once more than a single fused kernel (7 instead of
 // 5 matrix products) in exchange for no fp32 atomic traffic on dQ.
 // Warps: 0..7 softmax (two warpgroups), 8 TMA producer, 9 MMA issuer (one
@@ -54,7 +57,6 @@
 namespace cpa {
 namespace {
 
-constexpr int D = 128;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -98,7 +100,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileRows = 128;
-constexpr int kTileBytes = kTileRows * D * 2;  // 32 KB: [128 rows][128 bf16], two 64-column regions
+// One [128 rows][HD] bf16 tile: HD/64 regions of 64 columns (16 KB each, 128-byte swizzle).
+template <int HD>
+constexpr int tile_bytes() { return kTileRows * HD * 2; }
 constexpr int kSegCap = 128;                   // segments per group kept in shared memory
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
@@ -121,29 +125,13 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t par, volatile i
   return __all_sync(0xffffffffu, ok);
 }
 
-// Copies one 128-value bf16 row (global, 16-byte aligned) into 64 TMEM columns
-// of this thread's lane, two values per column.  Zeros when `valid` is false.
-__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16* src, bool valid) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t r[32];
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      uint4 x = valid ? __ldg(reinterpret_cast<const uint4*>(src) + half * 8 + v) : make_uint4(0, 0, 0, 0);
-      r[4 * v] = x.x;
-      r[4 * v + 1] = x.y;
-      r[4 * v + 2] = x.z;
-      r[4 * v + 3] = x.w;
-    }
-    ptx::tmem_st32(taddr + half * 32, r);
-  }
-}
-
 // ====================================================================== dK / dV
 
 constexpr int A_QST = 2;  // Q/dO stages
 
+template <int HD>
 struct ALayout {
+  static constexpr int kTileBytes = tile_bytes<HD>();
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;            // A_QST stages
@@ -242,12 +230,14 @@ __device__ __forceinline__ int count_qtiles(const KSeg* segs, int nseg, const Ke
 
 // kWin: the sliding window is applied (a.window > 0); without it the window
 // terms fold away at compile time.  Same flag on the dQ kernel.
-template <bool kWin>
+template <int HD, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Schedule s,
                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using L = ALayout;
+  using L = ALayout<HD>;
+  constexpr int D = HD;
+  constexpr int kTileBytes = L::kTileBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -318,6 +308,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- producer (whole warp)
       if (lane == 0) {
+        (void)CP_DCHECK(k_row0 < a.k_rows, a.err);  // TMA clips; the check reports
         ptx::mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
         for (int r = 0; r < D / 64; ++r) {
           ptx::tma_load_2d(smem + L::kK + r * 16384, &tm_k, &bars->kv_full, hk * D + r * 64, k_row0);
@@ -333,6 +324,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         const int st = j % A_QST;
         if (j >= A_QST && !wait_all(&bars->q_empty[st], ((j / A_QST) - 1) & 1, abort_flag, a.err)) break;
         if (lane == 0) {
+          (void)CP_DCHECK(t.q_row >= 0 && t.q_row < a.q_rows, a.err);
           ptx::mbar_arrive_expect_tx(&bars->q_full[st], 2 * kTileBytes);
           for (int r = 0; r < D / 64; ++r) {
             ptx::tma_load_2d(smem + L::kQ + st * kTileBytes + r * 16384, &tm_q, &bars->q_full[st],
@@ -345,6 +337,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
         float* lse_st = lse_all + st * 2 * kTileRows;
         for (int cidx = lane; cidx < t.nq; cidx += 32) {
           const int64_t off = (int64_t)t.h * a.lse_ld + t.q_row + cidx;
+          if (!CP_DCHECK(off < a.lse_size, a.err)) continue;
           ptx::cp_async4(lse_st + cidx, a.lse + off);
           ptx::cp_async4(lse_st + kTileRows + cidx, a.delta + off);
         }
@@ -568,7 +561,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
     if (ok) ok = wait_all(&bars->done, 0, abort_flag, a.err);
     if (ok) {
       ptx::tc_fence_after();
-      const bool valid = r < nk_tile;
+      const bool valid = r < nk_tile && CP_DCHECK((int64_t)k_row0 + r < a.k_rows, a.err);
       const int64_t krow = (int64_t)(k_row0 + r) * a.k_ld + (int64_t)hk * D;
       float* dst = (wg == 0 ? a.dv_acc : a.dk_acc) + krow;  // warpgroup 0: dV, 1: dK
       void* out_bf = wg == 0 ? a.dv_out : a.dk_out;
@@ -604,27 +597,37 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
 
 // ====================================================================== dQ
 
-constexpr int B_KST = 3;  // K/V stages
+constexpr int B_KST = 3;      // K stages (K_j is last read by dQ_j, the last product of tile j)
+constexpr int B_VST = 2;      // V stages (V_j is last read by dP_j, two products earlier)
+constexpr int kSegCapB = 96;  // key runs kept in shared memory (the tiles take the rest)
 
+template <int HD>
 struct BLayout {
-  static constexpr int kK = 0;                          // B_KST stages
-  static constexpr int kV = kK + B_KST * kTileBytes;
-  static constexpr int kBar = kV + B_KST * kTileBytes;
-  static constexpr int kSeg = kBar + 256;  // the group's key runs (up to kSegCap)
-  static constexpr int kBytes = kSeg + kSegCap * (int)sizeof(KSeg);
+  static constexpr int kTileBytes = tile_bytes<HD>();
+  static constexpr int kQ = 0;                        // the CTA's query tile
+  static constexpr int kDO = kQ + kTileBytes;         // its dO tile
+  static constexpr int kK = kDO + kTileBytes;         // B_KST stages
+  static constexpr int kV = kK + B_KST * kTileBytes;  // B_VST stages
+  static constexpr int kBar = kV + B_VST * kTileBytes;
+  static constexpr int kSeg = kBar + 256;  // the group's key runs (up to kSegCapB)
+  static constexpr int kBytes = kSeg + kSegCapB * (int)sizeof(KSeg);
   static constexpr int kSmemRequest = kBytes + 1024;
 };
+static_assert(BLayout<128>::kSmemRequest <= 227 * 1024, "dQ kernel: shared memory per CTA");
 
 struct BBars {
-  uint64_t q_full;  // Q and dO copied into TMEM
-  uint64_t kv_full[B_KST], kv_empty[B_KST];  // K and V tile of a stage landed / released
-  uint64_t s_full, dp_full;  // S / dP of the current tile in TMEM
-  uint64_t s_free;           // the softmax has read S
-  uint64_t ds_full;          // dS written back
-  uint64_t done;             // every MMA of the CTA has completed
+  uint64_t q_full;                         // Q and dO tiles landed
+  uint64_t k_full[B_KST], k_empty[B_KST];  // K tile of a stage landed / released (after dQ_j)
+  uint64_t v_full[B_VST], v_empty[B_VST];  // V tile of a stage landed / released (after dP_j)
+  uint64_t s_full;      // S of the current tile in TMEM
+  uint64_t s_free;      // the softmax has read S
+  uint64_t dp_full[2];  // dP of tile j in buffer j % 2
+  uint64_t ds_full[2];  // dS of tile j written back over buffer j % 2
+  uint64_t done;        // every MMA of the CTA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(BBars) <= 256, "dQ kernel barriers");
 
 struct TileCtx {
   int64_t pq_lo, pq_hi;
@@ -694,11 +697,14 @@ __device__ __forceinline__ int count_ktiles(const KSeg* segs, int nseg, const Ti
   return n;
 }
 
-template <bool kWin>
+template <int HD, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Schedule s,
+                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using L = BLayout;
+  using L = BLayout<HD>;
+  constexpr int D = HD;
+  constexpr int kTileBytes = L::kTileBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -731,19 +737,25 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   // The group's key runs, read at every tile by every role: shared memory when they fit.
   const int nseg = seg_end - seg_begin;
   KSeg* seg_sm = reinterpret_cast<KSeg*>(smem + L::kSeg);
-  const KSeg* segs = nseg <= kSegCap ? seg_sm : &s.s[seg_begin];
-  if (nseg <= kSegCap)
+  const KSeg* segs = nseg <= kSegCapB ? seg_sm : &s.s[seg_begin];
+  if (nseg <= kSegCapB)
     for (int i = threadIdx.x; i < nseg; i += kThreads) seg_sm[i] = s.s[seg_begin + i];
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, kSoftmaxThreads);
+    ptx::mbar_init(&bars->q_full, 1);
     for (int i = 0; i < B_KST; ++i) {
-      ptx::mbar_init(&bars->kv_full[i], 1);
-      ptx::mbar_init(&bars->kv_empty[i], 1);
+      ptx::mbar_init(&bars->k_full[i], 1);
+      ptx::mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < B_VST; ++i) {
+      ptx::mbar_init(&bars->v_full[i], 1);
+      ptx::mbar_init(&bars->v_empty[i], 1);
     }
     ptx::mbar_init(&bars->s_full, 1);
-    ptx::mbar_init(&bars->dp_full, 1);
     ptx::mbar_init(&bars->s_free, kSoftmaxThreads);
-    ptx::mbar_init(&bars->ds_full, kSoftmaxThreads);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->dp_full[i], 1);
+      ptx::mbar_init(&bars->ds_full[i], kSoftmaxThreads);
+    }
     ptx::mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -753,6 +765,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     ptx::tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_do);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
   }
@@ -767,30 +781,47 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     if (warp == kProducerWarp) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
+        (void)CP_DCHECK((int64_t)q_row0 + i0 < a.q_rows, a.err);  // TMA clips; the check reports
+        ptx::mbar_arrive_expect_tx(&bars->q_full, 2 * kTileBytes);
+        for (int r = 0; r < D / 64; ++r) {
+          ptx::tma_load_2d(smem + L::kQ + r * 16384, &tm_q, &bars->q_full, h * D + r * 64, q_row0 + i0);
+          ptx::tma_load_2d(smem + L::kDO + r * 16384, &tm_do, &bars->q_full, h * D + r * 64, q_row0 + i0);
+        }
         KIter it;
         kiter_init(it, segs, nseg, c);
         int j = 0;
         KvTile t;
-        int issued[B_KST] = {0, 0, 0};
+        int issued_k[B_KST] = {0, 0, 0}, issued_v[B_VST] = {0, 0};
         while (!*abort_flag && kiter_next(it, c, t)) {
-          const int st = j % B_KST;
-          if (j >= B_KST && !ptx::mbar_wait_bounded(&bars->kv_empty[st], ((j / B_KST) - 1) & 1, abort_flag,
+          const int sk = j % B_KST, sv = j % B_VST;
+          (void)CP_DCHECK(t.k_row >= 0 && t.k_row < a.k_rows, a.err);
+          if (j >= B_KST && !ptx::mbar_wait_bounded(&bars->k_empty[sk], ((j / B_KST) - 1) & 1, abort_flag,
                                                      a.err, kWaitNs))
             break;
-          ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * kTileBytes);
-          for (int r = 0; r < D / 64; ++r) {
-            ptx::tma_load_2d(smem + L::kK + st * kTileBytes + r * 16384, &tm_k, &bars->kv_full[st],
+          ptx::mbar_arrive_expect_tx(&bars->k_full[sk], kTileBytes);
+          for (int r = 0; r < D / 64; ++r)
+            ptx::tma_load_2d(smem + L::kK + sk * kTileBytes + r * 16384, &tm_k, &bars->k_full[sk],
                              hk * D + r * 64, t.k_row);
-            ptx::tma_load_2d(smem + L::kV + st * kTileBytes + r * 16384, &tm_v, &bars->kv_full[st],
+          issued_k[sk] = j + 1;
+          if (j >= B_VST && !ptx::mbar_wait_bounded(&bars->v_empty[sv], ((j / B_VST) - 1) & 1, abort_flag,
+                                                     a.err, kWaitNs))
+            break;
+          ptx::mbar_arrive_expect_tx(&bars->v_full[sv], kTileBytes);
+          for (int r = 0; r < D / 64; ++r)
+            ptx::tma_load_2d(smem + L::kV + sv * kTileBytes + r * 16384, &tm_v, &bars->v_full[sv],
                              hk * D + r * 64, t.k_row);
-          }
-          issued[st] = j + 1;
+          issued_v[sv] = j + 1;
           ++j;
         }
         if (*abort_flag) {
+          (void)ptx::mbar_wait_bounded(&bars->q_full, 0, nullptr, nullptr, kDrainNs);
           for (int st = 0; st < B_KST; ++st)
-            if (issued[st] > 0)
-              (void)ptx::mbar_wait_bounded(&bars->kv_full[st], ((issued[st] - 1) / B_KST) & 1, nullptr,
+            if (issued_k[st] > 0)
+              (void)ptx::mbar_wait_bounded(&bars->k_full[st], ((issued_k[st] - 1) / B_KST) & 1, nullptr,
+                                           nullptr, kDrainNs);
+          for (int st = 0; st < B_VST; ++st)
+            if (issued_v[st] > 0)
+              (void)ptx::mbar_wait_bounded(&bars->v_full[st], ((issued_v[st] - 1) / B_VST) & 1, nullptr,
                                            nullptr, kDrainNs);
         }
       }
@@ -798,56 +829,65 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K^T, dO V^T (TMEM A)
+        constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K^T, dO V^T (shared memory)
         constexpr uint32_t id_q = ptx::idesc_bf16_f32(128, D, 0, 1);    // dS K (TMEM A)
         bool any = false;
         auto wait = [&](uint64_t* bar, uint32_t par) {
           return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
         };
-        auto scores = [&](uint32_t d, uint32_t a_tmem, uint32_t b_addr) {
+        auto scores = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + d, tmem + a_tmem + kk * 8, desc_k(b_addr, kk), id_s, kk > 0);
+            ptx::mma_bf16_ss(tmem + d, desc_k(a_addr, kk), desc_k(b_addr, kk), id_s, kk > 0);
         };
-        // Issue order S_{j+1}, dQ_j, dP_{j+1}; each gap between two products holds one
-        // barrier wait (tile j+2's K/V is waited for one tile ahead) and no schedule walking.
+        // dP / dS of tile j live in TMEM columns 128.. (j even) or 384.. (j odd), so
+        // dP_{j+1} is issued as soon as the softmax has read S_j, before dS_j exists.
+        // Issue order per tile: S_{j+1}, dP_{j+1}, dQ_j; each gap between two
+        // products holds one barrier wait (the loads' are normally complete: their
+        // test is the cheap path) and no schedule walking.
         const int n = count_ktiles(segs, nseg, c);
-        if (n > 0 && wait(&bars->q_full, 0) && wait(&bars->kv_full[0], 0)) {
+        bool ok = n > 0 && wait(&bars->q_full, 0) && wait(&bars->k_full[0], 0);
+        if (ok) {
           ptx::tc_fence_after();
-          scores(0, 384, sbase + L::kK);
+          scores(0, sbase + L::kQ, sbase + L::kK);
           ptx::tc_commit(&bars->s_full);
-          scores(128, 448, sbase + L::kV);
-          ptx::tc_commit(&bars->dp_full);
           any = true;
-          bool ok = n < 2 || wait(&bars->kv_full[1 % B_KST], (1 / B_KST) & 1);
-          for (int j = 0; ok && j < n; ++j) {
-            const int st = j % B_KST, st1 = (j + 1) % B_KST;
-            const bool more = j + 1 < n;
-            // next tile's S once the softmax has read this tile's S
-            if (more) {
-              if (!(ok = wait(&bars->s_free, j & 1))) break;
-              ptx::tc_fence_after();
-              scores(0, 384, sbase + L::kK + st1 * kTileBytes);
-              ptx::tc_commit(&bars->s_full);
-            }
-            // dQ += dS K once dS is written back (dS: two warpgroup halves of 64 keys)
-            if (!(ok = wait(&bars->ds_full, j & 1))) break;
+          ok = wait(&bars->v_full[0], 0);
+          if (ok) {
             ptx::tc_fence_after();
-            {
-              const uint32_t k_addr = sbase + L::kK + st * kTileBytes;
-#pragma unroll
-              for (int kk = 0; kk < kTileRows / 16; ++kk)
-                ptx::mma_bf16_ts(tmem + 256, a_split(tmem + 128, kk), desc_mn(k_addr, kk), id_q,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            ptx::tc_commit(&bars->kv_empty[st]);
-            // next tile's dP (reuses the dP columns after dQ has read dS)
-            if (more) {
-              scores(128, 448, sbase + L::kV + st1 * kTileBytes);
-              ptx::tc_commit(&bars->dp_full);
-              if (j + 2 < n) ok = wait(&bars->kv_full[(j + 2) % B_KST], ((j + 2) / B_KST) & 1);
-            }
+            scores(128, sbase + L::kDO, sbase + L::kV);
+            ptx::tc_commit(&bars->dp_full[0]);
+            ptx::tc_commit(&bars->v_empty[0]);
           }
+        }
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {
+            const int j1 = j + 1, sk1 = j1 % B_KST, sv1 = j1 % B_VST;
+            // S_{j+1} once the softmax has read S_j
+            if (!(ok = wait(&bars->s_free, j & 1))) break;
+            if (!(ok = wait(&bars->k_full[sk1], (j1 / B_KST) & 1))) break;
+            ptx::tc_fence_after();
+            scores(0, sbase + L::kQ, sbase + L::kK + sk1 * kTileBytes);
+            ptx::tc_commit(&bars->s_full);
+            // dP_{j+1} into the other buffer (dQ_{j-1}, which read it, is ahead in the pipe)
+            if (!(ok = wait(&bars->v_full[sv1], (j1 / B_VST) & 1))) break;
+            ptx::tc_fence_after();
+            scores(j1 & 1 ? 384 : 128, sbase + L::kDO, sbase + L::kV + sv1 * kTileBytes);
+            ptx::tc_commit(&bars->dp_full[j1 & 1]);
+            ptx::tc_commit(&bars->v_empty[sv1]);
+          }
+          // dQ += dS_j K_j once dS_j is written back (two warpgroup halves of 64 keys)
+          if (!(ok = wait(&bars->ds_full[j & 1], (j >> 1) & 1))) break;
+          ptx::tc_fence_after();
+          {
+            const uint32_t k_addr = sbase + L::kK + (j % B_KST) * kTileBytes;
+            const uint32_t ds = j & 1 ? 384 : 128;
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+              ptx::mma_bf16_ts(tmem + 256, a_split(tmem + ds, kk), desc_mn(k_addr, kk), id_q,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::tc_commit(&bars->k_empty[j % B_KST]);
         }
         if (any) {
           ptx::tc_commit(&bars->done);
@@ -867,23 +907,16 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const bool row_valid = r < nq_tile;
-    // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, once
-    {
-      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(w == 0 ? a.q : a.dout) +
-                                 (int64_t)(q_row0 + i0 + r) * a.q_ld + (int64_t)h * D;
-      row_to_tmem(lane_addr + 384 + w * 64, src, row_valid);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->q_full);
-    }
     const int64_t pq = c.pq_lo + (int64_t)qpos_st * r;
     int64_t st_r = 0, en_r = 0;
     if (c.docs && row_valid) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
     float nlse2 = 0.f, delta = 0.f;  // -lse*log2(e); rows without a visible key are fully masked
     if (row_valid) {
       const int64_t col = (int64_t)h * a.lse_ld + q_row0 + i0 + r;
-      nlse2 = -a.lse[col] * kLog2e;
-      delta = a.delta[col];
+      if (CP_DCHECK(col < a.lse_size, a.err)) {
+        nlse2 = -a.lse[col] * kLog2e;
+        delta = a.delta[col];
+      }
     }
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nl2x2 = ptx::f2_pack(nlse2, nlse2);
@@ -924,6 +957,8 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       ptx::tmem_ld32(lane_addr + cb + 32, sr2[1]);
       ptx::tmem_wait_ld_regs(sr2[0]);
       ptx::tmem_wait_ld_regs(sr2[1]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->s_free);  // S is in registers: the next S may overwrite it
 #pragma unroll
       for (int hc = 0; hc < 64; hc += 32) {
         const uint32_t* sr = sr2[hc / 32];
@@ -945,16 +980,15 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->s_free);
       // phase 2: dS = P o (dP - Delta), 32 columns at a time, packed over the dP columns
-      // already read
-      if (!wait_all(&bars->dp_full, j & 1, abort_flag, a.err)) { ok = false; break; }
+      // already read, in this tile's buffer
+      const uint32_t buf = j & 1 ? 384 : 128;
+      if (!wait_all(&bars->dp_full[j & 1], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       ptx::tc_fence_after();
 #pragma unroll
       for (int hc = 0; hc < 64; hc += 32) {
         uint32_t dr[32];
-        ptx::tmem_ld32(lane_addr + 128 + cb + hc, dr);
+        ptx::tmem_ld32(lane_addr + buf + cb + hc, dr);
         ptx::tmem_wait_ld_regs(dr);
         uint32_t dd[16];
         if (fast) {
@@ -976,11 +1010,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
             dd[cc / 2] = ptx::pack_bf16x2(ds0, ds1);
           }
         }
-        ptx::tmem_st16(lane_addr + 128 + cb + hc / 2, dd);
+        ptx::tmem_st16(lane_addr + buf + cb + hc / 2, dd);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->ds_full);
+      ptx::mbar_arrive(&bars->ds_full[j & 1]);
       ++j;
     }
     // ------------------------------------------------------------ dQ epilogue
@@ -992,7 +1026,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
       float* dst = a.dq_acc + qrow;
       __nv_bfloat16* dst_bf = a.dq_out ? static_cast<__nv_bfloat16*>(a.dq_out) + qrow : nullptr;
 #pragma unroll
-      for (int ch = w * 2; ch < w * 2 + 2; ++ch) {  // 64 columns per warpgroup
+      for (int ch = w * (D / 64); ch < (w + 1) * (D / 64); ++ch) {  // D/2 columns per warpgroup
         uint32_t rr[32];
         if (j > 0) {
           ptx::tmem_ld32(lane_addr + 256 + ch * 32, rr);
@@ -1001,7 +1035,9 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = 0u;
         }
-        if (row_valid && dst_bf) {
+        if (!CP_DCHECK(!row_valid || (int64_t)q_row0 + i0 + r < a.q_rows, a.err)) {
+          // out of the q rows: skipped (debug builds)
+        } else if (row_valid && dst_bf) {
           store_row_bf16(dst_bf + ch * 32, rr, a.scale);
         } else if (row_valid) {
           store_row_f32(dst + ch * 32, rr, a.scale, a.accumulate);
@@ -1111,19 +1147,13 @@ bool invert_schedule(const Schedule& km, Schedule& qm) {
   return true;
 }
 
-}  // namespace
-
-cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
-                             cudaStream_t st) {
-  if (a.D != D) {
-    set_last_error("tcgen05 attention backward supports D = 128");
-    return CP_ERR_UNSUPPORTED;
-  }
+template <int HD>
+cp_status launch_typed(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows, cudaStream_t st) {
   // setmaxnreg.inc waits until the registers it asks for are free in the block's launch
   // budget, so launch only if each kernel's compiled register count covers the split.
   const bool win = a.window > 0;
-  auto dkdv_kernel = win ? attn_bwd_dkdv_kernel<true> : attn_bwd_dkdv_kernel<false>;
-  auto dq_kernel = win ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
+  auto dkdv_kernel = win ? attn_bwd_dkdv_kernel<HD, true> : attn_bwd_dkdv_kernel<HD, false>;
+  auto dq_kernel = win ? attn_bwd_dq_kernel<HD, true> : attn_bwd_dq_kernel<HD, false>;
   for (const void* kfn : {(const void*)dkdv_kernel, (const void*)dq_kernel}) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kfn);
@@ -1136,19 +1166,19 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   }
   CUtensorMap mq, mdo, mk, mv;
   cp_status r;
-  if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * D)) != CP_OK) return r;
-  if ((r = make_map(&mdo, a.dout, q_rows, (int64_t)a.Hq * D)) != CP_OK) return r;
-  if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * D)) != CP_OK) return r;
-  if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * D)) != CP_OK) return r;
+  if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * HD)) != CP_OK) return r;
+  if ((r = make_map(&mdo, a.dout, q_rows, (int64_t)a.Hq * HD)) != CP_OK) return r;
+  if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * HD)) != CP_OK) return r;
+  if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * HD)) != CP_OK) return r;
 
   // dK / dV over the key-major schedule
   int64_t units = schedule_units(s, kTileRows, a.Hkv);
   schedule_order(s, kTileRows, kTileRows, true, a.causal, a.window, a.cu_seqlens != nullptr);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ALayout::kSmemRequest);
+                                         ALayout<HD>::kSmemRequest);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dkdv)");
-    dkdv_kernel<<<(unsigned)units, kThreads, ALayout::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
+    dkdv_kernel<<<(unsigned)units, kThreads, ALayout<HD>::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
     if ((r = cuda_check(cudaGetLastError(), "attn_bwd_dkdv_kernel launch")) != CP_OK) return r;
   }
   // dQ over the query-major schedule (same pairs)
@@ -1162,16 +1192,26 @@ cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int6
   schedule_order(*qm, kTileRows, kTileRows, false, a.causal, a.window, a.cu_seqlens != nullptr);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         BLayout::kSmemRequest);
+                                         BLayout<HD>::kSmemRequest);
     if (e != cudaSuccess) {
       delete qm;
       return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dq)");
     }
-    dq_kernel<<<(unsigned)units, kThreads, BLayout::kSmemRequest, st>>>(a, *qm, mk, mv);
+    dq_kernel<<<(unsigned)units, kThreads, BLayout<HD>::kSmemRequest, st>>>(a, *qm, mq, mdo, mk, mv);
     r = cuda_check(cudaGetLastError(), "attn_bwd_dq_kernel launch");
   }
   delete qm;
   return r;
+}
+
+}  // namespace
+
+cp_status launch_attn_bwd_tc(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows,
+                             cudaStream_t st) {
+  if (a.D == 128) return launch_typed<128>(a, s, q_rows, k_rows, st);
+  if (a.D == 64) return launch_typed<64>(a, s, q_rows, k_rows, st);
+  set_last_error("tcgen05 attention backward supports D = 64 or 128");
+  return CP_ERR_UNSUPPORTED;
 }
 
 }  // namespace cpa

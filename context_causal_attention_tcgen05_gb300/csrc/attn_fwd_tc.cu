@@ -223,6 +223,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   int issued[2] = {0, 0};
   auto issue_kv = [&](const KvTile& t) {
     const int st = pj & 1;
+    (void)CP_DCHECK(t.k_row >= 0 && t.k_row < a.k_rows, a.err);
     ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::kTile);
 #pragma unroll
     for (int r = 0; r < D / 64; ++r) {
@@ -266,6 +267,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      (void)CP_DCHECK((int64_t)q_row0 + i0 < a.q_rows, a.err);  // TMA clips; the check reports
       ptx::mbar_arrive_expect_tx(&bars->q_full, (has1 ? 2 : 1) * L::kTile);
       for (int w = 0; w < (has1 ? 2 : 1); ++w)
 #pragma unroll
@@ -514,7 +516,8 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
         // bf16 output of a warp whose 32 rows are all valid: staged in this query tile's
         // Q buffer (free once o_done fired) in the 128-byte swizzled layout of the O
         // tensor map, then written by one TMA store per 64 columns.
-        const bool staged = !kOutF32 && a.o_tma && quad * 32 + 32 <= nq_w;
+        const bool staged = !kOutF32 && a.o_tma && quad * 32 + 32 <= nq_w &&
+                            CP_DCHECK((int64_t)s.g[g].o_row0 + i0 + w * BM + quad * 32 + 32 <= a.q_rows, a.err);
         if (staged) {
           uint8_t* stg = smem + L::kQ + w * L::kTile + quad * (32 * D * 2);
 #pragma unroll
@@ -561,7 +564,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
 #pragma unroll
             for (int i = 0; i < 32; ++i) rr[i] = 0u;
           }
-          if (valid) {
+          if (valid && CP_DCHECK((int64_t)s.g[g].o_row0 + i0 + w * BM + r < a.q_rows, a.err)) {
             if (kOutF32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + ch * 32);
 #pragma unroll
@@ -587,9 +590,10 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
             }
           }
         }
-        if (valid) {
+        const int64_t li = (int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + w * BM + r;
+        if (valid && CP_DCHECK(li < a.lse_size, a.err)) {
           const float Lr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-          a.lse[(int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + w * BM + r] = Lr;
+          a.lse[li] = Lr;
         }
         if (staged && lane == 0) ptx::bulk_wait_group_read0();  // the CTA's smem outlives the reads
       }

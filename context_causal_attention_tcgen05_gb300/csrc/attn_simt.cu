@@ -65,8 +65,9 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
   for (int e = threadIdx.x; e < kFwdRows * D; e += 128) {
     int r = e / D, d = e - r * D;
     int i = i0 + r;
-    qs[e] = (i < grp.nq) ? load_as_f32(q + (int64_t)(grp.q_row0 + i) * a.q_ld + (int64_t)h * D + d)
-                         : 0.f;
+    qs[e] = (i < grp.nq && CP_DCHECK((int64_t)grp.q_row0 + i < a.q_rows, a.err))
+                ? load_as_f32(q + (int64_t)(grp.q_row0 + i) * a.q_ld + (int64_t)h * D + d)
+                : 0.f;
   }
 
   // Per row state (4 rows per warp).
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
         int r = e / D, d = e - r * D;
         int j = j0 + r;
         float kv = 0.f, vv = 0.f;
-        if (j < seg.nk) {
+        if (j < seg.nk && CP_DCHECK((int64_t)seg.k_row0 + j < a.k_rows, a.err)) {
           int64_t off = (int64_t)(seg.k_row0 + j) * a.k_ld + (int64_t)hk * D + d;
           kv = load_as_f32(k + off);
           vv = load_as_f32(v + off);
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
   for (int r = 0; r < 4; ++r) {
     int i = i0 + warp + 4 * r;
     if (i >= grp.nq) continue;
+    if (!CP_DCHECK((int64_t)grp.o_row0 + i < a.q_rows, a.err)) continue;
     float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
     int64_t orow = (int64_t)(grp.o_row0 + i) * a.o_ld + (int64_t)h * D;
 #pragma unroll
@@ -157,9 +159,10 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
           store_from_f32(o + orow + d, acc[r][c] * inv);
       }
     }
-    if (lane == 0) {
+    const int64_t li = (int64_t)(grp.lse_head0 + h) * a.lse_ld + grp.lse_col0 + i;
+    if (lane == 0 && CP_DCHECK(li < a.lse_size, a.err)) {
       float L = l[r] > 0.f ? (m[r] + log2f(l[r])) * kLn2 : -INFINITY;
-      a.lse[(int64_t)(grp.lse_head0 + h) * a.lse_ld + grp.lse_col0 + i] = L;
+      a.lse[li] = L;
     }
   }
 }
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(BwdArgs a, Schedule 
     int r = e / D, d = e - r * D;
     int j = j0 + r;
     float kv = 0.f, vv = 0.f;
-    if (j < kg.nq) {
+    if (j < kg.nq && CP_DCHECK((int64_t)kg.q_row0 + j < a.k_rows, a.err)) {
       int64_t off = (int64_t)(kg.q_row0 + j) * a.k_ld + (int64_t)hk * D + d;
       kv = load_as_f32(k + off);
       vv = load_as_f32(v + off);
@@ -215,6 +218,8 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(BwdArgs a, Schedule 
       const KSeg qs = s.s[kg.seg_begin + si];  // query run
       for (int i = warp; i < qs.nk; i += 4) {
         const int64_t qrow_idx = (int64_t)(qs.k_row0 + i);
+        if (!CP_DCHECK(qrow_idx < a.q_rows && (int64_t)h * a.lse_ld + qrow_idx < a.lse_size, a.err))
+          continue;  // warp-uniform
         const int64_t pq = (int64_t)qs.pos_off + (int64_t)qs.pos_stride * i;
         __syncwarp();
         for (int d = lane; d < D; d += 32) {
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(BwdArgs a, Schedule 
   for (int e = threadIdx.x; e < kKT * D; e += 128) {
     int r = e / D, d = e - r * D;
     int jj = j0 + r;
-    if (jj < kg.nq) {
+    if (jj < kg.nq && CP_DCHECK((int64_t)kg.q_row0 + jj < a.k_rows, a.err)) {
       int64_t off = (int64_t)(kg.q_row0 + jj) * a.k_ld + (int64_t)hk * D + d;
       a.dk_acc[off] = dks[r * Dp + d] + (a.accumulate ? a.dk_acc[off] : 0.f);
       a.dv_acc[off] = dvs[r * Dp + d] + (a.accumulate ? a.dv_acc[off] : 0.f);

@@ -78,6 +78,9 @@ struct AttnArgs {
   int32_t o_f32;      // output dtype: 1 fp32, 0 same as input
   int32_t o_tma;      // bf16 output written by TMA stores through the launch's O tensor map
   int32_t window;     // sliding window (causal only): pos_q - pos_k < window; 0 = none
+  // Buffer extents, for the index checks of debug builds: rows of q (and o) and of
+  // k / v, and floats in the lse array.
+  int64_t q_rows, k_rows, lse_size;
 };
 
 // Backward extras.
@@ -109,12 +112,16 @@ struct BwdArgs {
   int32_t window;      // sliding window (causal only): pos_q - pos_k < window; 0 = none
   int32_t accumulate;  // fp32 outputs: add into the values already there (each row is still
                        // written by one CTA, so no atomics); 0 = overwrite
+  // Buffer extents, for the index checks of debug builds: rows of q / dout / dq and
+  // of k / v / dk / dv, and floats in the lse (and Delta) array.
+  int64_t q_rows, k_rows, lse_size;
 };
 
 // Device error codes written into the error word (first writer wins).
 enum DeviceError : int32_t {
   kDevOk = 0,
   kDevTimeout = 1,
+  kDevIndex = 2,  // debug builds: an index check failed (the access was skipped)
 };
 
 // ---------------------------------------------------------------- host side helpers (api.cu)
@@ -210,7 +217,7 @@ enum GatherKind : int {
   kZigzagRestoreCols = 8,  // as 16-byte runs (needs S/(2P) % 4 == 0)
 };
 
-// True when the backward runs on the tensor-core kernels (bf16, D = 128), which
+// True when the backward runs on the tensor-core kernels (bf16, D = 64 or 128), which
 // write bf16 gradients directly (BwdArgs::dq_out etc.).
 bool bwd_writes_bf16(int32_t dtype, int32_t D);
 // True when none of the n_out output ranges overlaps any of the n_in input ranges
@@ -246,6 +253,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void record_device_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
+
+// Index checks of debug builds (compiled with -DCP_DEBUG): CP_DCHECK(cond, err) is
+// true when cond holds; otherwise it records kDevIndex in the error word and is
+// false, and the caller skips the access.  Release builds compile it to true.
+__device__ __forceinline__ bool debug_check(bool ok, int32_t* err) {
+  if (!ok) record_device_error(err, kDevIndex);
+  return ok;
+}
+#ifdef CP_DEBUG
+#define CP_DCHECK(cond, err) (::cpa::debug_check((cond), (err)))
+#else
+#define CP_DCHECK(cond, err) (true)
+#endif
 
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

@@ -34,6 +34,8 @@ struct GatherParams {
   uint32_t a;          // kind-specific: zigzag -> P; striped -> S/P; ulysses -> S
   uint32_t b;          // replicated seq2head: Hkv
   int kind;
+  uint32_t in_vec;     // input vectors (index checks of debug builds)
+  int32_t* err;        // device error word
 };
 
 // Several gathers in one launch: blocks [block0[i], block0[i+1]) serve gather i.
@@ -104,7 +106,10 @@ __global__ void __launch_bounds__(kThreads) row_gather_kernel(const __grid_const
       uint32_t u = i / p.run_vec;
       uint32_t w = i - u * p.run_vec;
       uint64_t src = (uint64_t)source_run(p, u) * p.run_vec + w;
-      buf[k] = __ldcs(p.x + src);
+      if (CP_DCHECK(src < p.in_vec, p.err))
+        buf[k] = __ldcs(p.x + src);
+      else
+        dst[k] = 0xffffffffu;  // debug builds: out-of-range source, nothing stored
     }
   }
 #pragma unroll
@@ -118,6 +123,7 @@ struct LsePermParams {
   float* y;
   uint32_t S, P, H, C;
   int kind;
+  int32_t* err;  // device error word (index checks of debug builds)
 };
 
 __device__ __forceinline__ uint32_t lse_source_col(const LsePermParams& p, uint32_t col) {
@@ -147,20 +153,22 @@ __global__ void __launch_bounds__(256) lse_permute_kernel(LsePermParams p) {
   uint64_t total = (uint64_t)p.S * p.H;
   for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total; t += (uint64_t)gridDim.x * 256) {
     uint32_t h = (uint32_t)(t / p.S), col = (uint32_t)(t - (uint64_t)h * p.S);
-    p.y[t] = p.x[(uint64_t)h * p.S + lse_source_col(p, col)];
+    const uint32_t sc = lse_source_col(p, col);
+    if (CP_DCHECK(sc < p.S, p.err)) p.y[t] = p.x[(uint64_t)h * p.S + sc];
   }
 }
 
 // lse-shaped [H, S] fp32 -> the Ulysses head-major order [H/P][P*S]: rank p's
 // heads h' = 0..H/P-1 become heads of one P*S-row problem (row p*S + s).
 __global__ void __launch_bounds__(256) lse_heads_kernel(const float* x, float* y, uint32_t S, uint32_t P,
-                                                        uint32_t Hp, uint64_t total) {
+                                                        uint32_t Hp, uint64_t total, int32_t* err) {
   for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total; t += (uint64_t)gridDim.x * 256) {
     const uint64_t PS = (uint64_t)P * S;
     const uint32_t hp = (uint32_t)(t / PS);
     const uint64_t rem = t - (uint64_t)hp * PS;
     const uint32_t rank = (uint32_t)(rem / S), s = (uint32_t)(rem - (uint64_t)rank * S);
-    y[t] = x[((uint64_t)rank * Hp + hp) * S + s];
+    const uint64_t src = ((uint64_t)rank * Hp + hp) * S + s;
+    if (CP_DCHECK(src < total, err)) y[t] = x[src];
   }
 }
 
@@ -170,7 +178,8 @@ __global__ void __launch_bounds__(256) lse_heads_kernel(const float* x, float* y
 template <bool kBf16>
 __global__ void __launch_bounds__(256) heads_to_seq_sum_kernel(const float* src, void* dst, uint32_t S,
                                                                uint32_t Hd, uint32_t R, uint32_t Hp,
-                                                               uint32_t D, uint64_t total_vec) {
+                                                               uint32_t D, uint64_t total_vec, uint64_t src_elems,
+                                                               int32_t* err) {
   constexpr uint32_t kEpv = kBf16 ? 8 : 4;  // elements per 16-byte output vector
   const uint32_t vpr = D / kEpv;            // vectors per head row
   for (uint64_t t = blockIdx.x * 256ull + threadIdx.x; t < total_vec; t += (uint64_t)gridDim.x * 256) {
@@ -182,8 +191,9 @@ __global__ void __launch_bounds__(256) heads_to_seq_sum_kernel(const float* src,
     for (uint32_t e = 0; e < kEpv; ++e) acc[e] = 0.f;
     for (uint32_t r = 0; r < R; ++r) {
       const uint32_t g = hd * R + r, rank = g / Hp, hp = g - rank * Hp;
-      const float4* sp = reinterpret_cast<const float4*>(
-          src + (((uint64_t)rank * S + s) * Hp + hp) * D + (uint64_t)dv * kEpv);
+      const uint64_t off = (((uint64_t)rank * S + s) * Hp + hp) * D + (uint64_t)dv * kEpv;
+      if (!CP_DCHECK(off + kEpv <= src_elems, err)) continue;
+      const float4* sp = reinterpret_cast<const float4*>(src + off);
 #pragma unroll
       for (uint32_t e = 0; e < kEpv / 4; ++e) {
         const float4 f = __ldcs(sp + e);
@@ -237,6 +247,7 @@ cp_status fill_gather(const GatherJob& j, GatherParams& p) {
   p.P = (uint32_t)j.P;
   p.b = 0;
   p.kind = j.kind;
+  p.err = device_error_word();
   uint64_t total_bytes = (uint64_t)j.S * (uint64_t)j.row_bytes;
   uint64_t total_vec = total_bytes / 16;
   if (total_vec >= (1ull << 32)) {
@@ -244,6 +255,7 @@ cp_status fill_gather(const GatherJob& j, GatherParams& p) {
     return CP_ERR_UNSUPPORTED;
   }
   p.total_vec = (uint32_t)total_vec;
+  p.in_vec = (uint32_t)total_vec;  // the maps are permutations
   switch (j.kind) {
     case kZigzagReorder:
     case kZigzagRestore:
@@ -297,7 +309,9 @@ cp_status launch_kv_replicate(const void* x, void* y, int64_t S, int32_t Hkv, in
   p.a = (uint32_t)S;
   p.b = (uint32_t)Hkv;
   p.kind = kSeq2HeadRep;
+  p.err = device_error_word();
   p.run_vec = (uint32_t)(head_bytes / 16);
+  p.in_vec = (uint32_t)((uint64_t)S * Hkv * p.run_vec);  // each head of the input once
   const uint64_t total_vec = (uint64_t)P * S * p.run_vec;  // every rank's copy
   if (total_vec >= (1ull << 32)) {
     set_last_error("tensor larger than 64 GiB is not supported by the permute kernels");
@@ -312,7 +326,8 @@ cp_status launch_lse_to_heads(const float* x, float* y, int64_t S, int32_t H, in
   if (S == 0 || H == 0) return CP_OK;
   const uint64_t total = (uint64_t)S * H;
   const uint32_t blocks = (uint32_t)std::min<uint64_t>((total + 255) / 256, 152ull * 16);
-  lse_heads_kernel<<<blocks, 256, 0, st>>>(x, y, (uint32_t)S, (uint32_t)P, (uint32_t)(H / P), total);
+  lse_heads_kernel<<<blocks, 256, 0, st>>>(x, y, (uint32_t)S, (uint32_t)P, (uint32_t)(H / P), total,
+                                           device_error_word());
   return cuda_check(cudaGetLastError(), "lse_heads_kernel launch");
 }
 
@@ -321,13 +336,14 @@ cp_status launch_heads_to_seq_sum(const float* src, void* dst, int64_t S, int32_
   if (S == 0) return CP_OK;
   const uint64_t total_vec = (uint64_t)S * Hd * (D / (is_bf16 ? 8 : 4));
   const uint32_t blocks = (uint32_t)std::min<uint64_t>((total_vec + 255) / 256, 152ull * 32);
-  (void)P;
+  const uint64_t src_elems = (uint64_t)P * S * Hp * D;
+  int32_t* err = device_error_word();
   if (is_bf16)
     heads_to_seq_sum_kernel<true><<<blocks, 256, 0, st>>>(src, dst, (uint32_t)S, (uint32_t)Hd, (uint32_t)R,
-                                                          (uint32_t)Hp, (uint32_t)D, total_vec);
+                                                          (uint32_t)Hp, (uint32_t)D, total_vec, src_elems, err);
   else
     heads_to_seq_sum_kernel<false><<<blocks, 256, 0, st>>>(src, dst, (uint32_t)S, (uint32_t)Hd, (uint32_t)R,
-                                                           (uint32_t)Hp, (uint32_t)D, total_vec);
+                                                           (uint32_t)Hp, (uint32_t)D, total_vec, src_elems, err);
   return cuda_check(cudaGetLastError(), "heads_to_seq_sum_kernel launch");
 }
 
@@ -349,6 +365,7 @@ cp_status launch_lse_permute(int kind, const float* x, float* y, int64_t S, int3
   p.H = (uint32_t)H;
   p.C = (kind == kZigzagReorder || kind == kZigzagRestore) ? (uint32_t)(S / (2 * P)) : 0;
   p.kind = kind;
+  p.err = device_error_word();
   uint64_t total = (uint64_t)S * H;
   uint32_t blocks = (uint32_t)std::min<uint64_t>((total + 255) / 256, 152ull * 16);
   lse_permute_kernel<<<blocks, 256, 0, st>>>(p);

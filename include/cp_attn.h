@@ -55,7 +55,9 @@ typedef enum {
   CP_ERR_UNSUPPORTED = -5,    /* valid in principle but not provided (e.g. packing with contiguous ring) */
   CP_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than cp_workspace_size() */
   CP_ERR_CUDA = -7,           /* a CUDA runtime call failed (launch error, ...) */
-  CP_ERR_DEVICE_TIMEOUT = -8  /* a kernel's bounded wait expired (reported by cp_check_device_status) */
+  CP_ERR_DEVICE_TIMEOUT = -8, /* a kernel's bounded wait expired (reported by cp_check_device_status) */
+  CP_ERR_DEVICE_INDEX = -9    /* library built with CP_DEBUG: a kernel's index check failed and the
+                                 access was skipped (reported by cp_check_device_status) */
 } cp_status;
 
 typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
@@ -150,8 +152,8 @@ CP_API cp_status cp_attn_block_bwd(const void* q, const void* k, const void* v, 
                             void* workspace, size_t ws_bytes, void* stream);
 
 /* The same backward with gradients in the input dtype, overwritten (no
- * accumulation): dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype`.  For bf16 with
- * D = 128 the tensor-core kernels write them directly; gradients that share
+ * accumulation): dq [Sq,Hq,D], dk/dv [Sk,Hkv,D] in `dtype`.  For bf16 (D = 64
+ * or 128) the tensor-core kernels write them directly; gradients that share
  * storage with an input are still correct (then fp32 accumulators in the
  * workspace are cast after the kernels, as on the FFMA path).
  *   workspace: >= cp_workspace_size(CP_OP_BLOCK_BWD, ...) bytes (Delta and fp32
@@ -357,7 +359,8 @@ CP_API cp_status cp_workspace_size(int32_t op, int64_t S, int32_t Hq, int32_t Hk
 
 /* Synchronises `stream`, then reports (and clears) the library's device error
  * word: CP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the
- * last check, CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK. */
+ * last check, CP_ERR_DEVICE_INDEX if a debug build's index check failed,
+ * CP_ERR_CUDA if the stream holds a CUDA error, else CP_OK. */
 CP_API cp_status cp_check_device_status(void* stream);
 
 /* Test hook for the bounded-wait path: launches one block that waits on a
