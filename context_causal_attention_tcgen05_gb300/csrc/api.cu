@@ -518,7 +518,23 @@ cp_status ring_core(const void* q_re, const void* k_re, const void* v_re, void* 
   const float scale = 1.0f / sqrtf((float)D);
   Schedule* s = new Schedule;
   cp_status result = CP_OK;
-  if (mode == CP_RING_FUSED) {
+  if (mode == CP_RING_FUSED && layout == CP_REORDER_STRIPED && dtype == CP_BF16 && D == 128 &&
+      (P == 4 || P == 8 || P == 16)) {
+    // Striped, position-tiled: every rank's rows are in this GPU's memory, so the
+    // kernel tiles by position (a tile = 128/P rows of each rank, 128 consecutive
+    // positions) instead of by rank; the online softmax still merges every key
+    // block a query row sees, and the result is the ring's.  Each query tile then
+    // meets one causal diagonal instead of one per source rank.
+    s->n_groups = 0;
+    s->n_segs = 0;
+    add_group(*s, Piece{0, (int32_t)S, 0, 1});
+    add_seg(*s, Piece{0, (int32_t)S, 0, 1});
+    AttnArgs a = make_fwd_args(q_re, k_re, v_re, o_re, lse_re, Hq, Hkv, D, S, 1, cu_seqlens,
+                               n_docs, scale, 0);
+    a.perm_p = P;
+    a.perm_n = (int32_t)(S / P);
+    result = launch_fwd(a, *s, dtype, S, S, st);
+  } else if (mode == CP_RING_FUSED) {
     build_ring_schedule(*s, S, P, layout, -1, 1);
     AttnArgs a = make_fwd_args(q_re, k_re, v_re, o_re, lse_re, Hq, Hkv, D, S, 1, cu_seqlens,
                                n_docs, scale, 0);

@@ -178,8 +178,12 @@ __device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
 }
 
 // kWin: the sliding window is applied (a.window > 0); without it the window
-// terms fold away at compile time.
-template <int D, bool kOutF32, bool kWin>
+// terms fold away at compile time.  kP > 0: position-tiled striped buffers of kP
+// ranks (AttnArgs::perm_p): the schedule's rows are positions, every tile is
+// loaded as one 3-D TMA box of 128/kP rows of each rank (128 consecutive
+// positions), and shared-memory row r of a tile holds position
+// start + (r % (128/kP)) * kP + r / (128/kP).
+template <int D, bool kOutF32, bool kWin, int kP>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Schedule s,
                    const __grid_constant__ CUtensorMap tm_q,
@@ -187,6 +191,8 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_o) {
   using L = Layout<D>;
+  constexpr int kM = kP > 0 ? BM / kP : 1;  // rows of each rank in a tile (position-tiled)
+  static_assert(kP == 0 || (BM % kP == 0 && kP >= 4 && kP <= 16), "position tiles: 4 <= kP <= 16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -227,10 +233,17 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
     ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::kTile);
 #pragma unroll
     for (int r = 0; r < D / 64; ++r) {
-      ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
-                       hk * D + r * 64, t.k_row);
-      ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
-                       hk * D + r * 64, t.k_row);
+      if constexpr (kP > 0) {  // 128 consecutive positions: kM rows of every rank
+        ptx::tma_load_3d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
+                         hk * D + r * 64, t.k_row / kP, 0);
+        ptx::tma_load_3d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
+                         hk * D + r * 64, t.k_row / kP, 0);
+      } else {
+        ptx::tma_load_2d(smem + L::kK + st * L::kTile + r * 16384, &tm_k, &bars->kv_full[st],
+                         hk * D + r * 64, t.k_row);
+        ptx::tma_load_2d(smem + L::kV + st * L::kTile + r * 16384, &tm_v, &bars->kv_full[st],
+                         hk * D + r * 64, t.k_row);
+      }
     }
     issued[st] = pj + 1;
     ++pj;
@@ -271,9 +284,14 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       ptx::mbar_arrive_expect_tx(&bars->q_full, (has1 ? 2 : 1) * L::kTile);
       for (int w = 0; w < (has1 ? 2 : 1); ++w)
 #pragma unroll
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_2d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
-                           h * D + r * 64, q_row0 + i0 + w * BM);
+        for (int r = 0; r < D / 64; ++r) {
+          if constexpr (kP > 0)
+            ptx::tma_load_3d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
+                             h * D + r * 64, (q_row0 + i0 + w * BM) / kP, 0);
+          else
+            ptx::tma_load_2d(smem + L::kQ + w * L::kTile + r * 16384, &tm_q, &bars->q_full,
+                             h * D + r * 64, q_row0 + i0 + w * BM);
+        }
       TileIter pit;
       iter_init(pit, segs, nseg, cta, causal, docs);
       KvTile t;
@@ -395,9 +413,11 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       SpanCtx mine;
       const int64_t pq_lo_w = cta.pq_lo + (int64_t)qpos_st * (w * BM);
       span_init(mine, a, window, pq_lo_w, pq_lo_w + (int64_t)qpos_st * (nq_w - 1));
-      const int64_t pq = pq_lo_w + (int64_t)qpos_st * r;
+      // position of this thread's row (its offset in the tile's position window)
+      const int r_off = kP > 0 ? (r % kM) * kP + r / kM : r;
+      const int64_t pq = pq_lo_w + (int64_t)qpos_st * r_off;
       int64_t st_r = 0, en_r = 0;
-      if (docs && r < nq_w) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
+      if (docs && r_off < nq_w) doc_bounds(a.cu_seqlens, a.n_docs, pq, &st_r, &en_r);
       // first key position the row sees: its document's start and its window's start
       const int64_t first_r = max(docs ? st_r : INT64_MIN, window > 0 ? pq - window + 1 : INT64_MIN);
       const float sl2 = a.scale_log2;
@@ -443,9 +463,12 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
             for (int i = 0; i < 32; ++i) sv[ch * 32 + i] = __uint_as_float(rr[ch][i]);
           }
         }
-        if (!full) {
+        if (!full) {  // [ilo, ihi]: visible offsets in the key tile's position window
 #pragma unroll
-          for (int i = 0; i < BN; ++i) sv[i] = (i >= ilo && i <= ihi) ? sv[i] : -INFINITY;
+          for (int i = 0; i < BN; ++i) {
+            const int oi = kP > 0 ? (i % kM) * kP + i / kM : i;  // compile-time per column
+            sv[i] = (oi >= ilo && oi <= ihi) ? sv[i] : -INFINITY;
+          }
         }
         float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
@@ -510,14 +533,21 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
       if (ok) ok = wwait(&bars->o_done, 0);
       if (ok) {
         ptx::tc_fence_after();
-        const bool valid = r < nq_w;
+        const bool valid = r_off < nq_w;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        const int64_t orow = (int64_t)(s.g[g].o_row0 + i0 + w * BM + r) * a.o_ld + (int64_t)h * D;
+        // the buffer row of a tile row: rank r / kM, row tile_i0 + r % kM of that rank
+        // (position-tiled), else the schedule's row
+        const int32_t tile_i0 = kP > 0 ? (i0 + w * BM) / kP : 0;
+        auto buf_row = [&](int rr_) -> int64_t {
+          if constexpr (kP > 0) return (int64_t)(rr_ / kM) * a.perm_n + tile_i0 + rr_ % kM;
+          return (int64_t)s.g[g].o_row0 + i0 + w * BM + rr_;
+        };
+        const int64_t orow = buf_row(r) * a.o_ld + (int64_t)h * D;
         // bf16 output of a warp whose 32 rows are all valid: staged in this query tile's
         // Q buffer (free once o_done fired) in the 128-byte swizzled layout of the O
         // tensor map, then written by one TMA store per 64 columns.
-        const bool staged = !kOutF32 && a.o_tma && quad * 32 + 32 <= nq_w &&
-                            CP_DCHECK((int64_t)s.g[g].o_row0 + i0 + w * BM + quad * 32 + 32 <= a.q_rows, a.err);
+        const bool staged = !kOutF32 && a.o_tma && (kP > 0 ? nq_w == BM : quad * 32 + 32 <= nq_w) &&
+                            CP_DCHECK(kP > 0 || buf_row(quad * 32 + 31) < a.q_rows, a.err);
         if (staged) {
           uint8_t* stg = smem + L::kQ + w * L::kTile + quad * (32 * D * 2);
 #pragma unroll
@@ -548,9 +578,17 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            const int32_t y0 = s.g[g].o_row0 + i0 + w * BM + quad * 32;
+            if constexpr (kP > 0) {  // the warp's 32 rows: 32/kM ranks of kM rows, or 32 rows of one rank
+              const int32_t y0 = tile_i0 + (kM >= 32 ? (quad * 32) % kM : 0);
+              const int32_t z0 = (quad * 32) / kM;
 #pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) ptx::tma_store_2d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0);
+              for (int hf = 0; hf < D / 64; ++hf)
+                ptx::tma_store_3d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0, z0);
+            } else {
+              const int32_t y0 = s.g[g].o_row0 + i0 + w * BM + quad * 32;
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf) ptx::tma_store_2d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0);
+            }
             ptx::bulk_commit_group();
           }
         }
@@ -564,7 +602,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
 #pragma unroll
             for (int i = 0; i < 32; ++i) rr[i] = 0u;
           }
-          if (valid && CP_DCHECK((int64_t)s.g[g].o_row0 + i0 + w * BM + r < a.q_rows, a.err)) {
+          if (valid && CP_DCHECK(buf_row(r) < a.q_rows, a.err)) {
             if (kOutF32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + ch * 32);
 #pragma unroll
@@ -590,7 +628,8 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
             }
           }
         }
-        const int64_t li = (int64_t)(s.g[g].lse_head0 + h) * a.lse_ld + s.g[g].lse_col0 + i0 + w * BM + r;
+        const int64_t li = (int64_t)(s.g[g].lse_head0 + h) * a.lse_ld +
+                           (kP > 0 ? buf_row(r) : (int64_t)s.g[g].lse_col0 + i0 + w * BM + r);
         if (valid && CP_DCHECK(li < a.lse_size, a.err)) {
           const float Lr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
           a.lse[li] = Lr;
@@ -652,11 +691,35 @@ cp_status make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
   return CP_OK;
 }
 
-template <int D, bool kOutF32, bool kWin>
+// 3-D map over a striped buffer [P][n][cols] bf16 (rank-major): box 64 columns x
+// box_rows rows x box_ranks ranks, 128-byte swizzle.  A box of 128/P rows of all P
+// ranks holds 128 consecutive positions.
+cp_status make_map_striped(CUtensorMap* m, const void* base, int64_t n, int64_t P, int64_t cols, int box_rows,
+                           int box_ranks) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) {
+    set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
+    return CP_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)(n > 0 ? n : 1), (cuuint64_t)P};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * (cuuint64_t)n};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_ranks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled (striped) failed (code " + std::to_string((int)r) + ")");
+    return CP_ERR_CUDA;
+  }
+  return CP_OK;
+}
+
+template <int D, bool kOutF32, bool kWin, int kP = 0>
 cp_status launch_typed(const AttnArgs& a, Schedule& s, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mo, int64_t units, cudaStream_t st) {
   using L = Layout<D>;
-  auto kern = attn_fwd_tc_kernel<D, kOutF32, kWin>;
+  auto kern = attn_fwd_tc_kernel<D, kOutF32, kWin, kP>;
   // setmaxnreg.inc waits until the registers it asks for are free in the block's
   // launch budget, so launch only if the split fits that budget.
   cudaFuncAttributes fa;
@@ -685,6 +748,26 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
   }
   CUtensorMap mq, mk, mv;
   cp_status r;
+  if (a.perm_p > 0) {
+    // position-tiled striped buffers (bf16 output, D = 128, no window): every map is
+    // 3-D over [P][n][H*D]; the O map's box is one warp's 32 rows
+    const int P = a.perm_p, M = BM / P;
+    if (!(a.D == 128 && !a.o_f32 && a.window == 0 && (P == 4 || P == 8 || P == 16))) {
+      set_last_error("position-tiled striped forward: D = 128, bf16 output, P in {4, 8, 16}");
+      return CP_ERR_UNSUPPORTED;
+    }
+    CUtensorMap mo;
+    if ((r = make_map_striped(&mq, a.q, a.perm_n, P, (int64_t)a.Hq * a.D, M, P)) != CP_OK) return r;
+    if ((r = make_map_striped(&mk, a.k, a.perm_n, P, (int64_t)a.Hkv * a.D, M, P)) != CP_OK) return r;
+    if ((r = make_map_striped(&mv, a.v, a.perm_n, P, (int64_t)a.Hkv * a.D, M, P)) != CP_OK) return r;
+    if ((r = make_map_striped(&mo, a.o, a.perm_n, P, a.o_ld, M >= 32 ? 32 : M, M >= 32 ? 1 : 32 / M)) != CP_OK)
+      return r;
+    AttnArgs ao = a;
+    ao.o_tma = 1;
+    if (P == 4) return launch_typed<128, false, false, 4>(ao, s, mq, mk, mv, mo, units, st);
+    if (P == 8) return launch_typed<128, false, false, 8>(ao, s, mq, mk, mv, mo, units, st);
+    return launch_typed<128, false, false, 16>(ao, s, mq, mk, mv, mo, units, st);
+  }
   if ((r = make_map(&mq, a.q, q_rows, (int64_t)a.Hq * a.D)) != CP_OK) return r;
   if ((r = make_map(&mk, a.k, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;
   if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * a.D)) != CP_OK) return r;

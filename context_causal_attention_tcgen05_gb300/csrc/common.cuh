@@ -81,6 +81,10 @@ struct AttnArgs {
   // Buffer extents, for the index checks of debug builds: rows of q (and o) and of
   // k / v, and floats in the lse array.
   int64_t q_rows, k_rows, lse_size;
+  // Position-tiled striped buffers (perm_p > 0): q, k, v, o are [perm_p][perm_n][H*D]
+  // (rank r's row i holds position i*perm_p + r) and the schedule's rows are
+  // positions; a tile of 128 positions is 128/perm_p rows of every rank.
+  int32_t perm_p, perm_n;
 };
 
 // Backward extras.

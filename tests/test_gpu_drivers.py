@@ -425,3 +425,25 @@ def test_block_bwd_accumulate_flag_adds_and_overwrites():
     for t, g in zip(typed, base):
         assert torch.equal(t, g.to(torch.bfloat16))
     check_ok()
+
+
+@pytest.mark.parametrize("S,P,docs", [(800, 8, False), (800, 16, True), (1000, 4, True), (4096, 8, True),
+                                      (2048, 16, False)])
+def test_ring_striped_position_tiles(S, P, docs):
+    """The fused striped ring tiles by position (each tile = 128/P rows of every
+    rank, read as one 3-D box): ragged tails (S not a multiple of 128), every
+    compiled P, with and without packed documents, against unpartitioned attention."""
+    Hq, Hkv, D = 4, 2, 128
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=25)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 400, seed=9)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu)
+    o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, "striped", "fused", cu_seqlens=cu_d)
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"striped position tiles S={S} P={P}")
+    # the same buffers in the ranks' layout through the reordered entry point
+    qr, kr, vr = (cpa.cp_striped_reorder(x.cuda(), P) for x in (q, k, v))
+    o2, l2 = cpa.cp_ring_attention_reordered(qr, kr, vr, P, "striped", "fused", cu_seqlens=cu_d)
+    o2 = cpa.cp_striped_restore(o2, P)
+    l2 = cpa.cp_lse_reorder(l2, P, "striped", inverse=True)
+    assert_close(o2, l2, ref_o, ref_l, torch.bfloat16, f"striped reordered S={S} P={P}")
+    check_ok()
