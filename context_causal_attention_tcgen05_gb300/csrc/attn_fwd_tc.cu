@@ -66,6 +66,7 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s when draining after an ab
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSegCap = 128;                  // segments per group kept in shared memory
+constexpr int64_t kL2KvBytes = 32ll << 20;    // K/V bytes the launch order keeps in flight
 
 template <int D>
 struct Layout {
@@ -200,8 +201,17 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   const uint32_t sbase = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Launch order: blocks of head_block heads (whole key/value heads); within a block
+  // every (group, tile) pair in the schedule's order, the block's heads fastest, so
+  // the CTAs resident together read the key/value tiles of a few heads through L2.
   int g, tile, h;
-  decode_unit(s, kRowsPerCta, a.Hq, blockIdx.x, &g, &tile, &h);
+  {
+    const int hb = a.head_block, per_block = hb * (a.total_units / a.Hq);
+    const int u = blockIdx.x, b = u / per_block, rem = u - b * per_block, pair = rem / hb;
+    int h_unused;
+    decode_unit(s, kRowsPerCta, 1, pair, &g, &tile, &h_unused);
+    h = b * hb + (rem - pair * hb);
+  }
   const int hk = h / (a.Hq / a.Hkv);
   const int32_t window = kWin ? a.window : 0;
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
@@ -746,6 +756,26 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
     set_last_error("too many query tiles for one launch");
     return CP_ERR_UNSUPPORTED;
   }
+  // Heads per block of the launch order: the most whole key/value heads (a divisor
+  // of Hkv, at least one) whose K and V fit kL2KvBytes together.  This pays when
+  // every group reads most of the key rows (the ring, one block pair).  When groups
+  // read disjoint rows (Ulysses' ranks), or with packed documents (a unit reads
+  // only its documents' keys), one block (every head fastest) measured faster.
+  AttnArgs ab = a;
+  {
+    int64_t keys_max = 0;
+    for (int i = 0; i < s.n_groups; ++i) {
+      int64_t n = 0;
+      for (int j = s.g[i].seg_begin; j < s.g[i].seg_begin + s.g[i].seg_count; ++j) n += s.s[j].nk;
+      keys_max = std::max(keys_max, n);
+    }
+    const int64_t kv_bytes = std::max<int64_t>(1, k_rows * (int64_t)a.D * 2 * 2);
+    int kb = (int)std::min<int64_t>(a.Hkv, std::max<int64_t>(1, kL2KvBytes / kv_bytes));
+    if (a.cu_seqlens || 2 * keys_max < k_rows) kb = a.Hkv;
+    while (a.Hkv % kb) --kb;
+    ab.head_block = kb * (a.Hq / a.Hkv);
+    ab.total_units = (int32_t)units;
+  }
   CUtensorMap mq, mk, mv;
   cp_status r;
   if (a.perm_p > 0) {
@@ -762,7 +792,7 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
     if ((r = make_map_striped(&mv, a.v, a.perm_n, P, (int64_t)a.Hkv * a.D, M, P)) != CP_OK) return r;
     if ((r = make_map_striped(&mo, a.o, a.perm_n, P, a.o_ld, M >= 32 ? 32 : M, M >= 32 ? 1 : 32 / M)) != CP_OK)
       return r;
-    AttnArgs ao = a;
+    AttnArgs ao = ab;
     ao.o_tma = 1;
     if (P == 4) return launch_typed<128, false, false, 4>(ao, s, mq, mk, mv, mo, units, st);
     if (P == 8) return launch_typed<128, false, false, 8>(ao, s, mq, mk, mv, mo, units, st);
@@ -775,7 +805,7 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
   // (fp32 output, or a base the tensor map cannot take) rows are stored directly.
   CUtensorMap mo;
   memset(&mo, 0, sizeof(mo));
-  AttnArgs ao = a;
+  AttnArgs ao = ab;
   ao.o_tma = 0;
   if (!a.o_f32) {
     int64_t o_rows = 0;

@@ -85,6 +85,9 @@ struct AttnArgs {
   // (rank r's row i holds position i*perm_p + r) and the schedule's rows are
   // positions; a tile of 128 positions is 128/perm_p rows of every rank.
   int32_t perm_p, perm_n;
+  // Forward launch order: units in blocks of head_block heads (whole key/value
+  // heads), each block's heads fastest; total_units = (group, tile) pairs x Hq.
+  int32_t head_block;
 };
 
 // Backward extras.
