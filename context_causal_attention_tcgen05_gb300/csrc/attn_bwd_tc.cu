@@ -247,7 +247,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
   float* lse_all = reinterpret_cast<float*>(smem + L::kLse);
 
   int g, tile, hk;
-  decode_unit(s, kTileRows, a.Hkv, blockIdx.x, &g, &tile, &hk);
+  decode_unit_blocked(s, kTileRows, a.kv_head_block, a.kv_pairs, blockIdx.x, &g, &tile, &hk);
   const int32_t k_row0 = s.g[g].q_row0 + tile * kTileRows;  // key-major schedule: group = key run
   const int nk_tile = min(kTileRows, s.g[g].nq - tile * kTileRows);
   const int seg_begin = s.g[g].seg_begin, seg_end = seg_begin + s.g[g].seg_count;
@@ -713,7 +713,7 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int g, tile, h;
-  decode_unit(s, kTileRows, a.Hq, blockIdx.x, &g, &tile, &h);
+  decode_unit_blocked(s, kTileRows, a.q_head_block, a.q_pairs, blockIdx.x, &g, &tile, &h);
   const int hk = h / (a.Hq / a.Hkv);
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
   const int32_t qpos_off = s.g[g].pos_off, qpos_st = s.g[g].pos_stride;
@@ -1147,6 +1147,26 @@ bool invert_schedule(const Schedule& km, Schedule& qm) {
   return true;
 }
 
+// Key/value heads per block of a backward launch order (decode_unit_blocked): the
+// most whole key/value heads, a divisor of Hkv, whose shared operand bytes (the
+// other side's rows a unit reads: Q and dO of the head's query heads for dK/dV, K
+// and V for dQ) fit kL2SharedBytes together.  Every head fastest (one block) when
+// the groups read disjoint rows of the other side (Ulysses' ranks) or with packed
+// documents, as in the forward.
+constexpr int64_t kL2SharedBytes = 128ll << 20;
+int kv_heads_per_block(const Schedule& s, const BwdArgs& a, int64_t other_rows, int64_t bytes_per_kv_head) {
+  int64_t other_max = 0;
+  for (int i = 0; i < s.n_groups; ++i) {
+    int64_t n = 0;
+    for (int j = s.g[i].seg_begin; j < s.g[i].seg_begin + s.g[i].seg_count; ++j) n += s.s[j].nk;
+    other_max = std::max(other_max, n);
+  }
+  if (a.cu_seqlens || 2 * other_max < other_rows) return a.Hkv;
+  int kb = (int)std::min<int64_t>(a.Hkv, std::max<int64_t>(1, kL2SharedBytes / std::max<int64_t>(1, bytes_per_kv_head)));
+  while (a.Hkv % kb) --kb;
+  return kb;
+}
+
 template <int HD>
 cp_status launch_typed(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_rows, cudaStream_t st) {
   // setmaxnreg.inc waits until the registers it asks for are free in the block's launch
@@ -1172,13 +1192,16 @@ cp_status launch_typed(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_
   if ((r = make_map(&mv, a.v, k_rows, (int64_t)a.Hkv * HD)) != CP_OK) return r;
 
   // dK / dV over the key-major schedule
+  BwdArgs ab = a;
   int64_t units = schedule_units(s, kTileRows, a.Hkv);
   schedule_order(s, kTileRows, kTileRows, true, a.causal, a.window, a.cu_seqlens != nullptr);
+  ab.kv_pairs = (int32_t)(units / a.Hkv);
+  ab.kv_head_block = kv_heads_per_block(s, a, q_rows, (int64_t)(a.Hq / a.Hkv) * HD * 2 * 2 * q_rows);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          ALayout<HD>::kSmemRequest);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dkdv)");
-    dkdv_kernel<<<(unsigned)units, kThreads, ALayout<HD>::kSmemRequest, st>>>(a, s, mq, mdo, mk, mv);
+    dkdv_kernel<<<(unsigned)units, kThreads, ALayout<HD>::kSmemRequest, st>>>(ab, s, mq, mdo, mk, mv);
     if ((r = cuda_check(cudaGetLastError(), "attn_bwd_dkdv_kernel launch")) != CP_OK) return r;
   }
   // dQ over the query-major schedule (same pairs)
@@ -1190,6 +1213,8 @@ cp_status launch_typed(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_
   }
   units = schedule_units(*qm, kTileRows, a.Hq);
   schedule_order(*qm, kTileRows, kTileRows, false, a.causal, a.window, a.cu_seqlens != nullptr);
+  ab.q_pairs = (int32_t)(units / a.Hq);
+  ab.q_head_block = (a.Hq / a.Hkv) * kv_heads_per_block(*qm, a, k_rows, (int64_t)HD * 2 * 2 * k_rows);
   if (units > 0) {
     cudaError_t e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          BLayout<HD>::kSmemRequest);
@@ -1197,7 +1222,7 @@ cp_status launch_typed(const BwdArgs& a, Schedule& s, int64_t q_rows, int64_t k_
       delete qm;
       return cuda_check(e, "cudaFuncSetAttribute(attn_bwd_dq)");
     }
-    dq_kernel<<<(unsigned)units, kThreads, BLayout<HD>::kSmemRequest, st>>>(a, *qm, mq, mdo, mk, mv);
+    dq_kernel<<<(unsigned)units, kThreads, BLayout<HD>::kSmemRequest, st>>>(ab, *qm, mq, mdo, mk, mv);
     r = cuda_check(cudaGetLastError(), "attn_bwd_dq_kernel launch");
   }
   delete qm;

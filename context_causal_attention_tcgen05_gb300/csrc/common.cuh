@@ -122,6 +122,9 @@ struct BwdArgs {
   // Buffer extents, for the index checks of debug builds: rows of q / dout / dq and
   // of k / v / dk / dv, and floats in the lse (and Delta) array.
   int64_t q_rows, k_rows, lse_size;
+  // Launch orders (decode_unit_blocked): (group, tile) pairs of the key-major and the
+  // query-major schedule, and heads per block of each launch.
+  int32_t kv_pairs, q_pairs, kv_head_block, q_head_block;
 };
 
 // Device error codes written into the error word (first writer wins).
@@ -402,6 +405,21 @@ __device__ __forceinline__ void decode_unit(const Schedule& s, int tile_rows, in
   *g_out = g;
   *tile_out = ntiles - 1 - local;  // heaviest (last) tiles of a group first
   *h_out = h;
+}
+
+// Unit u of a launch ordered in blocks of head_block heads: the block is
+// u / (head_block * pairs); inside it the (group, tile) pairs come in the launch
+// order table's (else the default) order with the block's heads fastest, so the
+// CTAs resident together share the other side's rows of a few heads in L2.
+// head_block = heads gives the plain order (every head fastest).
+__device__ __forceinline__ void decode_unit_blocked(const Schedule& s, int tile_rows, int head_block,
+                                                    int pairs, int u, int* g_out, int* tile_out,
+                                                    int* h_out) {
+  const int per_block = head_block * pairs;
+  const int b = u / per_block, rem = u - b * per_block, pair = rem / head_block;
+  int h0;
+  decode_unit(s, tile_rows, 1, pair, g_out, tile_out, &h0);
+  *h_out = b * head_block + (rem - pair * head_block);
 }
 
 }  // namespace cpa
