@@ -1153,7 +1153,11 @@ bool invert_schedule(const Schedule& km, Schedule& qm) {
 // and V for dQ) fit kL2SharedBytes together.  Every head fastest (one block) when
 // the groups read disjoint rows of the other side (Ulysses' ranks) or with packed
 // documents, as in the forward.
+#ifndef CP_DEBUG
 constexpr int64_t kL2SharedBytes = 128ll << 20;
+#else
+constexpr int64_t kL2SharedBytes = 1;  // debug build: one key/value head per block at any size
+#endif
 int kv_heads_per_block(const Schedule& s, const BwdArgs& a, int64_t other_rows, int64_t bytes_per_kv_head) {
   int64_t other_max = 0;
   for (int i = 0; i < s.n_groups; ++i) {

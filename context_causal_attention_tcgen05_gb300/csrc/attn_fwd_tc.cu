@@ -66,7 +66,11 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s when draining after an ab
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when the max grows by > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSegCap = 128;                  // segments per group kept in shared memory
+#ifndef CP_DEBUG
 constexpr int64_t kL2KvBytes = 32ll << 20;    // K/V bytes the launch order keeps in flight
+#else
+constexpr int64_t kL2KvBytes = 1;             // debug build: one key/value head per block at any size
+#endif
 
 template <int D>
 struct Layout {

@@ -1,7 +1,10 @@
 """Runs in a child process with CP_ATTN_LIBRARY naming the index-checking debug
 build (libcp_attn_debug.so): every kernel family on small ragged cases, each
-result against the oracle, and the device status after each.  Exits 0 when all
-results meet their bounds and no index check fired; prints one line per check."""
+result against the oracle, and the device status after each.  That build also
+orders every attention launch in blocks of one key/value head, so the blocked
+unit orders that release builds use at large sizes run here at small ones.
+Exits 0 when all results meet their bounds and no index check fired; prints one
+line per check."""
 import os
 import sys
 
@@ -64,6 +67,19 @@ def main():
             g = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, layout, cu_seqlens=cu_d)
             for name, got, ref in zip(("dq", "dk", "dv"), g, (rq, rk, rv)):
                 check(f"ring bwd {layout} D={D} {name}", err(got, ref), 2e-2 * max(1.0, float(np.abs(ref).max())))
+    # ring without documents (GQA, both layouts): the debug build orders every launch in
+    # blocks of one key/value head, so the blocked unit orders run element by element here
+    S, Hq, Hkv, D, P = 2048, 8, 2, 128, 4
+    q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=34, with_dout=True)
+    ro, rl = oracle.attention(q, k, v, True)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, True)
+    for layout in ("zigzag", "contiguous"):
+        o, l = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout)
+        check(f"ring {layout} gqa out", err(o, ro), 2e-2)
+        check(f"ring {layout} gqa lse", err(l, rl), 5e-3)
+        g = cpa.cp_ring_attention_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, do.cuda(), P, layout)
+        for name, got, ref in zip(("dq", "dk", "dv"), g, (rq, rk, rv)):
+            check(f"ring bwd {layout} gqa {name}", err(got, ref), 2e-2 * max(1.0, float(np.abs(ref).max())))
     # Ulysses with replicated key/value heads and a window, fwd + bwd
     S, Hq, Hkv, D, P, W = 512, 8, 2, 128, 4, 100
     q, k, v, do = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=32, with_dout=True)
