@@ -105,14 +105,17 @@ template <int HD>
 constexpr int tile_bytes() { return kTileRows * HD * 2; }
 constexpr int kSegCap = 128;                   // segments per group kept in shared memory
 
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
-  // K-major, 128B swizzle: K step of 16 bf16 = 32 bytes inside a 64-column (16 KB) region.
-  return ptx::smem_desc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+// Operand descriptors as a tile's base descriptor plus a compile-time step per K
+// slice (the start-address field counts 16-byte units in its low 14 bits, and
+// shared memory ends below 2^18 bytes, so the step never carries out of it).
+// K-major, 128B swizzle: K step of 16 bf16 = 32 bytes inside a 64-column (16 KB) region.
+__device__ __forceinline__ uint64_t desc_k_base(uint32_t base) { return ptx::smem_desc_sw128(base, 16, 1024); }
+__device__ __forceinline__ constexpr uint64_t desc_k_step(int kk) {
+  return (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
 }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
-  // MN-major, 128B swizzle: K step of 16 rows of 128 bytes; next 64 N columns at +16 KB.
-  return ptx::smem_desc_sw128(base + kk * (16 * 128), 16384, 1024);
-}
+// MN-major, 128B swizzle: K step of 16 rows of 128 bytes; next 64 N columns at +16 KB.
+__device__ __forceinline__ uint64_t desc_mn_base(uint32_t base) { return ptx::smem_desc_sw128(base, 16384, 1024); }
+__device__ __forceinline__ constexpr uint64_t desc_mn_step(int kk) { return (uint64_t)((kk * (16 * 128)) >> 4); }
 // TMEM A operand of K = 128 packed over two 64-column halves written by the two
 // warpgroups: K step kk (16 values = 8 columns) of half kk / 4.
 __device__ __forceinline__ uint32_t a_split(uint32_t base, int kk) {
@@ -364,14 +367,16 @@ attn_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ 
           return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
         };
         auto scores = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr) {
+          const uint64_t ad = desc_k_base(a_addr), bd = desc_k_base(b_addr);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + d, desc_k(a_addr, kk), desc_k(b_addr, kk), id_s, kk > 0);
+            ptx::mma_bf16_ss(tmem + d, ad + desc_k_step(kk), bd + desc_k_step(kk), id_s, kk > 0);
         };
         auto grads = [&](uint32_t d, uint32_t a_tmem, uint32_t b_addr, bool acc) {
+          const uint64_t bd = desc_mn_base(b_addr);
 #pragma unroll
           for (int kk = 0; kk < kTileRows / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + d, a_split(tmem + a_tmem, kk), desc_mn(b_addr, kk), id_kv,
+            ptx::mma_bf16_ts(tmem + d, a_split(tmem + a_tmem, kk), bd + desc_mn_step(kk), id_kv,
                              (acc || kk > 0) ? 1u : 0u);
         };
         const int n = count_qtiles(segs, nseg, c);  // no schedule walking between products
@@ -836,9 +841,10 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
           return ptx::mbar_wait_bounded(bar, par, abort_flag, a.err, kWaitNs);
         };
         auto scores = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr) {
+          const uint64_t ad = desc_k_base(a_addr), bd = desc_k_base(b_addr);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + d, desc_k(a_addr, kk), desc_k(b_addr, kk), id_s, kk > 0);
+            ptx::mma_bf16_ss(tmem + d, ad + desc_k_step(kk), bd + desc_k_step(kk), id_s, kk > 0);
         };
         // dP / dS of tile j live in TMEM columns 128.. (j even) or 384.. (j odd), so
         // dP_{j+1} is issued as soon as the softmax has read S_j, before dS_j exists.
@@ -880,11 +886,11 @@ attn_bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ Sc
           if (!(ok = wait(&bars->ds_full[j & 1], (j >> 1) & 1))) break;
           ptx::tc_fence_after();
           {
-            const uint32_t k_addr = sbase + L::kK + (j % B_KST) * kTileBytes;
+            const uint64_t kd = desc_mn_base(sbase + L::kK + (j % B_KST) * kTileBytes);
             const uint32_t ds = j & 1 ? 384 : 128;
 #pragma unroll
             for (int kk = 0; kk < kTileRows / 16; ++kk)
-              ptx::mma_bf16_ts(tmem + 256, a_split(tmem + ds, kk), desc_mn(k_addr, kk), id_q,
+              ptx::mma_bf16_ts(tmem + 256, a_split(tmem + ds, kk), kd + desc_mn_step(kk), id_q,
                                (j > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::tc_commit(&bars->k_empty[j % B_KST]);
