@@ -760,6 +760,9 @@ cp_status launch_attn_fwd_tc(const AttnArgs& a, Schedule& s, int64_t q_rows, int
     set_last_error("too many query tiles for one launch");
     return CP_ERR_UNSUPPORTED;
   }
+  // Inside each block of heads, the (group, tile) pairs that see the most key tiles
+  // start first (when the causal rule or a window sets the weights).
+  schedule_order(s, kRowsPerCta, BN, false, a.causal, a.window, a.cu_seqlens != nullptr);
   // Heads per block of the launch order: the most whole key/value heads (a divisor
   // of Hkv, at least one) whose K and V fit kL2KvBytes together.  This pays when
   // every group reads most of the key rows (the ring, one block pair).  When groups
