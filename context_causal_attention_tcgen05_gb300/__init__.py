@@ -28,7 +28,8 @@ __all__ = [
     "cp_ulysses_seq2head", "cp_ulysses_head2seq",
     "cp_zigzag_reorder", "cp_zigzag_restore", "cp_striped_reorder", "cp_striped_restore",
     "cp_lse_reorder", "cp_ring_reorder_qkv", "cp_ring_restore",
-    "cp_ring_attention", "cp_ring_attention_reordered", "cp_ring_attention_bwd", "cp_ulysses_attention",
+    "cp_ring_attention", "cp_ring_attention_reordered", "cp_ring_attention_reordered_to_seq",
+    "cp_ring_attention_bwd", "cp_ulysses_attention",
     "cp_ulysses_attention_bwd", "cp_usp_attention",
     "cp_workspace_size", "cp_check_device_status", "cp_debug_bounded_wait",
     "cp_status_string", "cp_last_error", "cp_version",
@@ -77,6 +78,8 @@ _SIGS = {
                           _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ring_attention_reordered": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                     _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_size, _c_p],
+    "cp_ring_attention_reordered_to_seq": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                           _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p],
     "cp_ring_attention_bwd": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32,
                               _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p],
     "cp_ulysses_attention": [_c_p, _c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p,
@@ -376,6 +379,23 @@ def cp_ring_attention(q, k, v, P, reorder="auto", mode="fused", cu_seqlens=None,
         _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P, REORDER[reorder], RING_MODE[mode],
         _ptr(cu_seqlens), n_docs, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+    return out, lse
+
+
+def cp_ring_attention_reordered_to_seq(q, k, v, P, reorder="zigzag", cu_seqlens=None, out=None, lse=None,
+                                       stream=None):
+    """Fused ring on inputs already in the ranks' layout (zigzag or contiguous); out and
+    lse come back in sequence order (the restore is done by the attention's writes)."""
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, S, dtype=torch.float32, device=q.device)
+    n_docs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check("cp_ring_attention_reordered_to_seq", load_library().cp_ring_attention_reordered_to_seq(
+        _ptr(q), _ptr(k), _ptr(v), S, Hq, Hkv, D, _dt(q), P, REORDER[reorder], _ptr(cu_seqlens), n_docs,
+        _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -254,14 +254,22 @@ void sort_groups_by_work(Schedule& s) {
   for (int i = 0; i < s.n_groups; ++i) s.g[i] = tmp[i];
 }
 
-// Ring schedule.  step < 0: every step (fused); else only that step.
-void build_ring_schedule(Schedule& s, int64_t S, int32_t P, int32_t layout, int step, int causal) {
+// Ring schedule.  step < 0: every step (fused); else only that step.  seq_out:
+// out rows and lse columns go to the pieces' sequence positions instead of their
+// rows in the ranks' layout (pieces of consecutive positions only), i.e. the
+// restore is done by the attention's own output writes.
+void build_ring_schedule(Schedule& s, int64_t S, int32_t P, int32_t layout, int step, int causal,
+                         bool seq_out = false) {
   auto pieces = rank_pieces(S, P, layout);
   s.n_groups = 0;
   s.n_segs = 0;
   for (int r = 0; r < P; ++r) {
     for (const Piece& q : pieces[r]) {
       add_group(s, q);
+      if (seq_out) {
+        s.g[s.n_groups - 1].o_row0 = q.pos_off;
+        s.g[s.n_groups - 1].lse_col0 = q.pos_off;
+      }
       for (int st = 0; st < P; ++st) {
         if (step >= 0 && st != step) continue;
         int src = ((r - st) % P + P) % P;
@@ -510,11 +518,14 @@ UlyssesBwdWs ulysses_bwd_ws(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32
 char* ws_at(void* base, size_t off) { return static_cast<char*>(base) + off; }
 
 // The ring over P virtual ranks on buffers already in the ranks' layout:
-// q/k/v/o rows in rank order, lse columns in rank order.
+// q/k/v rows in rank order; o rows and lse columns in rank order, or in sequence
+// order when seq_out (FUSED mode, zigzag or contiguous layout: every piece is a
+// run of consecutive positions, so the attention writes each row where the
+// restore would have put it).
 cp_status ring_core(const void* q_re, const void* k_re, const void* v_re, void* o_re, float* lse_re,
                     int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype, int32_t P,
                     int32_t layout, int32_t mode, const int32_t* cu_seqlens, int32_t n_docs,
-                    void* partials, const RingPartialsWs& w, cudaStream_t st) {
+                    void* partials, const RingPartialsWs& w, cudaStream_t st, bool seq_out = false) {
   const float scale = 1.0f / sqrtf((float)D);
   Schedule* s = new Schedule;
   cp_status result = CP_OK;
@@ -535,7 +546,7 @@ cp_status ring_core(const void* q_re, const void* k_re, const void* v_re, void* 
     a.perm_n = (int32_t)(S / P);
     result = launch_fwd(a, *s, dtype, S, S, st);
   } else if (mode == CP_RING_FUSED) {
-    build_ring_schedule(*s, S, P, layout, -1, 1);
+    build_ring_schedule(*s, S, P, layout, -1, 1, seq_out);
     AttnArgs a = make_fwd_args(q_re, k_re, v_re, o_re, lse_re, Hq, Hkv, D, S, 1, cu_seqlens,
                                n_docs, scale, 0);
     result = launch_fwd(a, *s, dtype, S, S, st);
@@ -1032,6 +1043,13 @@ cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t
   const int back_kind = layout == CP_REORDER_DUAL_CHUNK_SWAP ? kZigzagRestore : kStripedRestore;
   // Contiguous layout: rank r already holds rows [rC, (r+1)C) in place.
   const bool moved = layout != CP_REORDER_CONTIGUOUS;
+  // Zigzag with the fused ring: the attention writes out and lse in sequence order
+  // (each rank's chunks are runs of consecutive positions), so no restore pass.
+  const bool fused_restore = layout == CP_REORDER_DUAL_CHUNK_SWAP && mode == CP_RING_FUSED;
+  if (fused_restore) {
+    o_re = out;
+    lse_re = lse;
+  }
   if (moved) {
     GatherJob jobs[3] = {{fwd_kind, q, q_re, S, (int64_t)Hq * D * (int64_t)es, P},
                          {fwd_kind, k, k_re, S, (int64_t)Hkv * D * (int64_t)es, P},
@@ -1045,8 +1063,8 @@ cp_status cp_ring_attention(const void* q, const void* k, const void* v, int64_t
     lse_re = lse;
   }
   CP_TRY(ring_core(q_re, k_re, v_re, o_re, lse_re, S, Hq, Hkv, D, dtype, P, layout, mode,
-                   cu_seqlens, n_docs, ws_at(workspace, w.partials), w.pw, st));
-  if (moved) {
+                   cu_seqlens, n_docs, ws_at(workspace, w.partials), w.pw, st, fused_restore));
+  if (moved && !fused_restore) {
     GatherJob jobs[2] = {{back_kind, o_re, out, S, (int64_t)Hq * D * (int64_t)es, P}, {}};
     const int n = lse_cols_job(back_kind, lse_re, lse, S, Hq, P, jobs[1]) ? 2 : 1;
     CP_TRY(launch_row_gather_batch(jobs, n, st));
@@ -1080,6 +1098,27 @@ cp_status cp_ring_attention_reordered(const void* q, const void* k, const void* 
   CP_CHECK_T(lse, "lse", false);
   return ring_core(q, k, v, out, lse, S, Hq, Hkv, D, dtype, P, layout, mode, cu_seqlens, n_docs,
                    workspace, w, (cudaStream_t)stream);
+}
+
+cp_status cp_ring_attention_reordered_to_seq(const void* q, const void* k, const void* v, int64_t S,
+                                             int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                                             int32_t P, int32_t reorder, const int32_t* cu_seqlens,
+                                             int32_t n_docs, void* out, float* lse, void* stream) {
+  CP_REQUIRE(reorder >= CP_REORDER_CONTIGUOUS && reorder <= CP_REORDER_AUTO, CP_ERR_INVALID_ARG,
+             "reorder must be a cp_reorder value");
+  int32_t layout = resolve_layout(reorder, cu_seqlens);
+  CP_REQUIRE(layout != CP_REORDER_STRIPED, CP_ERR_UNSUPPORTED,
+             "sequence-order output needs runs of consecutive positions (zigzag or contiguous)");
+  CP_TRY(check_ring_args(S, Hq, Hkv, D, dtype, P, layout, cu_seqlens, n_docs));
+  if (S == 0) return CP_OK;
+  CP_CHECK_T(q, "q", false);
+  CP_CHECK_T(k, "k", false);
+  CP_CHECK_T(v, "v", false);
+  CP_CHECK_T(out, "out", false);
+  CP_CHECK_T(lse, "lse", false);
+  RingPartialsWs w = ring_partials_ws(S, Hq, D, CP_RING_FUSED);
+  return ring_core(q, k, v, out, lse, S, Hq, Hkv, D, dtype, P, layout, CP_RING_FUSED, cu_seqlens, n_docs,
+                   nullptr, w, (cudaStream_t)stream, true);
 }
 
 cp_status cp_ring_attention_bwd(const void* q, const void* k, const void* v, const void* out,

@@ -261,7 +261,8 @@ CP_API cp_status cp_ring_restore(const void* o_re, const float* lse_re, void* ou
  * layout of `reorder`).  q [S,Hq,D], k/v [S,Hkv,D], out [S,Hq,D] and lse [Hq,S]
  * are in ORIGINAL sequence order; the driver reorders q/k/v into the
  * workspace, runs the ring (skipping key blocks with no visible pair), and
- * restores out.  cu_seqlens (device, n_docs+1) packs documents; packing is
+ * restores out (for DUAL_CHUNK_SWAP with FUSED, the ring writes out and lse
+ * in sequence order directly, as cp_ring_attention_reordered_to_seq).  cu_seqlens (device, n_docs+1) packs documents; packing is
  * accepted only with a load-balanced layout (DUAL_CHUNK_SWAP, STRIPED or AUTO),
  * as in the MaxText packing PR.  Requires S % P == 0 (S % 2P for
  * DUAL_CHUNK_SWAP), 1 <= P <= 32.  workspace >= cp_workspace_size(CP_OP_RING_FWD). */
@@ -283,6 +284,18 @@ CP_API cp_status cp_ring_attention_reordered(const void* q, const void* k, const
                                              const int32_t* cu_seqlens, int32_t n_docs, void* out,
                                              float* lse, void* workspace, size_t ws_bytes,
                                              void* stream);
+
+/* cp_ring_attention_reordered in FUSED mode, with out [S,Hq,D] and lse [Hq,S]
+ * written in SEQUENCE order: the restore of cp_ring_attention is done by the
+ * attention's own output writes (each rank's pieces of the DUAL_CHUNK_SWAP and
+ * CONTIGUOUS layouts are runs of consecutive positions, so every output row is
+ * written once, at its sequence position).  q/k/v are in the ranks' layout as
+ * for cp_ring_attention_reordered; cu_seqlens is in sequence positions.  STRIPED
+ * (and AUTO with documents) returns CP_ERR_UNSUPPORTED.  No workspace. */
+CP_API cp_status cp_ring_attention_reordered_to_seq(const void* q, const void* k, const void* v, int64_t S,
+                                                    int32_t Hq, int32_t Hkv, int32_t D, int32_t dtype,
+                                                    int32_t P, int32_t reorder, const int32_t* cu_seqlens,
+                                                    int32_t n_docs, void* out, float* lse, void* stream);
 
 /* Backward of cp_ring_attention: dq [S,Hq,D], dk/dv [S,Hkv,D] (original
  * order) from the forward's out and lse and the upstream gradient dout.

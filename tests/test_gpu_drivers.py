@@ -86,6 +86,34 @@ def test_ring_bf16_packed_medium(layout):
     check_ok()
 
 
+@pytest.mark.parametrize("layout,docs", [("zigzag", False), ("zigzag", True), ("contiguous", False)])
+def test_ring_reordered_to_seq(layout, docs):
+    # the fused ring writing out and lse at their sequence positions (the restore done
+    # by the attention's own writes), on inputs in the ranks' layout; ragged chunks
+    # (C = 200 is not a multiple of the 128-row tile) and several heads per key head
+    S, Hq, Hkv, D, P = 1600, 8, 2, 128, 4
+    q, k, v = make_inputs(S, Hq, Hkv, D, torch.bfloat16, seed=9)
+    cu = cu_seqlens_from_lengths(doc_lengths(S, 64, 700, seed=5)) if docs else None
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    ref_o, ref_l = oracle.attention(q, k, v, True, cu_seqlens=cu)
+    reo = cpa.cp_zigzag_reorder if layout == "zigzag" else (lambda x, P: x)
+    qr, kr, vr = (reo(x.cuda(), P) for x in (q, k, v))
+    o, l = cpa.cp_ring_attention_reordered_to_seq(qr, kr, vr, P, layout, cu_seqlens=cu_d)
+    check_ok()
+    assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"to_seq {layout} docs={docs}")
+    # the driver takes the same path for zigzag + fused: identical results
+    o2, l2 = cpa.cp_ring_attention(q.cuda(), k.cuda(), v.cuda(), P, layout, "fused", cu_seqlens=cu_d)
+    check_ok()
+    assert torch.equal(o, o2) and torch.equal(l, l2)
+
+
+def test_ring_reordered_to_seq_refuses_striped():
+    q = torch.zeros(256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cpa.CpAttnError) as ei:
+        cpa.cp_ring_attention_reordered_to_seq(q, q, q, 4, "striped")
+    assert ei.value.status == -5  # CP_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("Hq,Hkv,P", [(8, 8, 4), (8, 4, 4), (16, 8, 8)])
 def test_ulysses_bf16_medium(Hq, Hkv, P):
     S, D = 1024, 128
