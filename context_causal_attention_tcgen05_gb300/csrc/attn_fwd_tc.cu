@@ -209,13 +209,7 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
   // every (group, tile) pair in the schedule's order, the block's heads fastest, so
   // the CTAs resident together read the key/value tiles of a few heads through L2.
   int g, tile, h;
-  {
-    const int hb = a.head_block, per_block = hb * (a.total_units / a.Hq);
-    const int u = blockIdx.x, b = u / per_block, rem = u - b * per_block, pair = rem / hb;
-    int h_unused;
-    decode_unit(s, kRowsPerCta, 1, pair, &g, &tile, &h_unused);
-    h = b * hb + (rem - pair * hb);
-  }
+  decode_unit_blocked(s, kRowsPerCta, a.head_block, a.total_units / a.Hq, blockIdx.x, &g, &tile, &h);
   const int hk = h / (a.Hq / a.Hkv);
   const int32_t window = kWin ? a.window : 0;
   const int32_t q_row0 = s.g[g].q_row0, nq = s.g[g].nq;
