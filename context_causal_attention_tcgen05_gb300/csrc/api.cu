@@ -1266,20 +1266,25 @@ cp_status cp_ulysses_attention(const void* q, const void* k, const void* v, int6
   Schedule* s = new Schedule;
   s->n_groups = 0;
   s->n_segs = 0;
+  // Rank p's attention writes its query heads straight into out's sequence layout
+  // (rows = positions, head columns p*Hqp ..): the head2seq of out is done by the
+  // attention's own output writes, as lse's is.
   for (int p = 0; p < P; ++p) {
     add_group(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
     s->g[p].lse_col0 = 0;
     s->g[p].lse_head0 = p * Hqp;
+    s->g[p].o_row0 = 0;
+    s->g[p].o_head0 = p * Hqp;
     add_seg(*s, Piece{(int32_t)(p * S), (int32_t)S, 0, 1});
   }
-  AttnArgs a = make_fwd_args(qh, kh, vh, oh, lse, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
+  (void)oh;
+  AttnArgs a = make_fwd_args(qh, kh, vh, out, lse, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
                              1.0f / sqrtf((float)D), 0);
+  a.o_ld = (int64_t)Hq * D;
   a.window = window;
   cp_status stt = launch_fwd(a, *s, dtype, (int64_t)P * S, (int64_t)P * S, st);
   delete s;
-  CP_TRY(stt);
-  CP_TRY(launch_row_gather(kHead2Seq, oh, out, S, (int64_t)Hq * D * es, P, Hq, st));
-  return CP_OK;
+  return stt;
 }
 
 cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t S, int32_t Hq,

@@ -550,7 +550,8 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
           if constexpr (kP > 0) return (int64_t)(rr_ / kM) * a.perm_n + tile_i0 + rr_ % kM;
           return (int64_t)s.g[g].o_row0 + i0 + w * BM + rr_;
         };
-        const int64_t orow = buf_row(r) * a.o_ld + (int64_t)h * D;
+        const int32_t oh = s.g[g].o_head0 + h;  // output head column block
+        const int64_t orow = buf_row(r) * a.o_ld + (int64_t)oh * D;
         // bf16 output of a warp whose 32 rows are all valid: staged in this query tile's
         // Q buffer (free once o_done fired) in the 128-byte swizzled layout of the O
         // tensor map, then written by one TMA store per 64 columns.
@@ -591,11 +592,11 @@ attn_fwd_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ S
               const int32_t z0 = (quad * 32) / kM;
 #pragma unroll
               for (int hf = 0; hf < D / 64; ++hf)
-                ptx::tma_store_3d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0, z0);
+                ptx::tma_store_3d(&tm_o, stg + hf * 4096, oh * D + hf * 64, y0, z0);
             } else {
               const int32_t y0 = s.g[g].o_row0 + i0 + w * BM + quad * 32;
 #pragma unroll
-              for (int hf = 0; hf < D / 64; ++hf) ptx::tma_store_2d(&tm_o, stg + hf * 4096, h * D + hf * 64, y0);
+              for (int hf = 0; hf < D / 64; ++hf) ptx::tma_store_2d(&tm_o, stg + hf * 4096, oh * D + hf * 64, y0);
             }
             ptx::bulk_commit_group();
           }

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnArgs a, Schedule
     if (i >= grp.nq) continue;
     if (!CP_DCHECK((int64_t)grp.o_row0 + i < a.q_rows, a.err)) continue;
     float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-    int64_t orow = (int64_t)(grp.o_row0 + i) * a.o_ld + (int64_t)h * D;
+    int64_t orow = (int64_t)(grp.o_row0 + i) * a.o_ld + (int64_t)(grp.o_head0 + h) * D;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       int d = lane + 32 * c;

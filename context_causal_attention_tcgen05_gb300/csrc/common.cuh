@@ -34,7 +34,8 @@ struct QGroup {
   int32_t lse_col0;    // lse column of row 0
   int32_t lse_head0;   // lse head (row of the [H, cols] lse) of head 0
   int32_t o_row0;      // first output row
-  int32_t pad0, pad1;
+  int32_t o_head0;     // output head offset: head h of the group goes to out column (o_head0 + h) * D
+  int32_t pad1;
 };
 
 // A run of key/value rows with one affine position map.
