@@ -82,6 +82,20 @@ def test_ring_refusals(lib):
     assert _ring(lib, ws=ctypes.c_void_p(0)) == -6
 
 
+def test_ring_to_seq_refusals(lib):
+    # sequence-order output needs runs of consecutive positions: striped (and AUTO with
+    # documents, which resolves to striped) is refused before any device work
+    f = lib.cp_ring_attention_reordered_to_seq
+    args = lambda S=8192, P=8, reorder=1, cu=None, n_docs=0: (
+        P16, P16, P16, S, 32, 32, 128, cpa.CP_BF16, P, reorder, cu, n_docs, P16, P16, None)
+    assert f(*args(reorder=2)) == -5
+    assert "consecutive positions" in cpa.cp_last_error()
+    assert f(*args(reorder=3, cu=P16, n_docs=3)) == -5
+    assert f(*args(S=8200)) == -2                          # S % 2P
+    assert f(*args(P=0)) == -1
+    assert f(*args(reorder=9)) == -1
+
+
 def test_ulysses_refusals(lib):
     f = lib.cp_ulysses_attention
     # q k v S Hq Hkv D dtype P cu n_docs window out lse ws ws_bytes stream
