@@ -1341,7 +1341,11 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
   // the fused ring across groups, once per head share, in one launch
   Schedule* ring = new Schedule;
   Schedule* s = new Schedule;
-  build_ring_schedule(*ring, S, P_ring, layout, -1, 1);
+  // Zigzag and contiguous ring pieces are runs of consecutive positions: the attention
+  // then writes out and lse at their final places (sequence rows, head share u's
+  // columns), so neither the head2seq nor the restore runs afterwards.
+  const bool direct = layout != CP_REORDER_STRIPED;
+  build_ring_schedule(*ring, S, P_ring, layout, -1, 1, direct);
   if ((int64_t)ring->n_groups * P_ulysses > kMaxGroups || (int64_t)ring->n_segs * P_ulysses > kMaxSegs) {
     delete ring;
     delete s;
@@ -1356,8 +1360,9 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
       QGroup& g = s->g[s->n_groups++];
       g = rg;
       g.q_row0 = rg.q_row0 + u * (int32_t)S;
-      g.o_row0 = rg.o_row0 + u * (int32_t)S;
-      g.lse_head0 = rg.lse_head0 + u * Hqp;  // lse columns stay in ring order
+      g.o_row0 = direct ? rg.o_row0 : rg.o_row0 + u * (int32_t)S;
+      g.o_head0 = direct ? u * Hqp : 0;
+      g.lse_head0 = rg.lse_head0 + u * Hqp;  // lse columns: sequence order when direct, else ring order
       g.seg_begin = s->n_segs;
       for (int si = 0; si < rg.seg_count; ++si) {
         KSeg sg = ring->s[rg.seg_begin + si];
@@ -1370,12 +1375,14 @@ cp_status cp_usp_attention(const void* q, const void* k, const void* v, int64_t 
   // outputs: head-major into the ring-ordered q buffer (free after seq2head, or never used
   // when the layout is contiguous), lse in ring order
   void* oh = ws_at(workspace, w.q_re);
-  float* lse_re = moved ? reinterpret_cast<float*>(ws_at(workspace, w.lse)) : lse;
-  AttnArgs a = make_fwd_args(qh, kh, vh, oh, lse_re, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
+  float* lse_re = (moved && !direct) ? reinterpret_cast<float*>(ws_at(workspace, w.lse)) : lse;
+  AttnArgs a = make_fwd_args(qh, kh, vh, direct ? out : oh, lse_re, Hqp, Hkvp, D, S, 1, cu_seqlens, n_docs,
                              1.0f / sqrtf((float)D), 0);
+  if (direct) a.o_ld = (int64_t)Hq * D;
   cp_status stt = launch_fwd(a, *s, dtype, (int64_t)P_ulysses * S, (int64_t)P_ulysses * S, st);
   delete s;
   CP_TRY(stt);
+  if (direct) return CP_OK;
   if (moved) {
     void* o_re = ws_at(workspace, w.qh);  // free after the attention
     CP_TRY(launch_row_gather(kHead2Seq, oh, o_re, S, (int64_t)Hq * D * es, P_ulysses, Hq, st));
